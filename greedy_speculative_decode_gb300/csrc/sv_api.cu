@@ -1,0 +1,737 @@
+// sv_api.cu -- the C-ABI: context, page pool and block table, step
+// orchestration (one CUDA graph per step shape, kernels chained with
+// programmatic dependent launch), and the synchronous / asynchronous calls.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "sv_internal.h"
+
+using namespace sv;
+
+struct GraphEntry {
+  int M, mode;
+  float* logits;
+  cudaGraphExec_t exec;
+};
+
+struct sv_ctx {
+  sv_config cfg;
+  int device = 0, num_sms = 0;
+  cudaStream_t user_stream = nullptr, stream = nullptr;
+  cudaEvent_t ev = nullptr;
+  bool use_graphs = true;
+  // weights
+  const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
+  std::vector<const bf16*> attn_norm, q_norm, k_norm, ffn_norm;
+  std::vector<LinearDesc> lin_qkv, lin_o, lin_gu, lin_down;
+  LinearDesc lin_head;
+  CUtensorMap kmap, vmap;
+  // device memory owned by the context
+  std::vector<void*> allocs;
+  bf16 *kpool = nullptr, *vpool = nullptr;
+  size_t layer_stride = 0;  // elements per layer in each pool
+  int* block_table = nullptr;
+  SvState* st = nullptr;
+  bf16 *x = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
+  float* x_ss = nullptr;
+  float2* rope = nullptr;
+  float2* part_ml = nullptr;
+  float* part_o = nullptr;
+  int max_splits = 0;
+  float* ws = nullptr;
+  int* counters = nullptr;
+  float* am_val = nullptr;
+  int* am_idx = nullptr;
+  // pinned host staging
+  int32_t* pin_in = nullptr;   // [cap_len, tokens...] per row block, max_seq + kMaxK + 1 slots
+  int32_t* pin_out = nullptr;  // result[4] + seq_len + status
+  int* pin_bt = nullptr;       // block table mirror
+  // host-side sequence state
+  int seq_len = 0;
+  int n_alloc = 0;  // logical pages with a physical page
+  int bt_len = 0;   // entries of the block table
+  std::vector<int> free_pages;
+  bool async_pending = false;
+  std::vector<GraphEntry> graphs;
+  std::string err;
+};
+
+namespace {
+
+int fail(sv_ctx* c, int code, const char* fmt, ...) {
+  if (c) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    c->err = buf;
+  }
+  return code;
+}
+
+#define CK(call)                                                                           \
+  do {                                                                                     \
+    cudaError_t e_ = (call);                                                               \
+    if (e_ != cudaSuccess)                                                                 \
+      return fail(ctx, SV_E_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));        \
+  } while (0)
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows, cols] row-major, box [box_rows, 64 cols], 128B swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Split of the K dimension: a function of the weight shape only, so every
+// row of every call sums its products in the same order.
+int choose_splits(int n_tiles, int Kd) {
+  const int kb = Kd / kLinBK;
+  int last_ok = 1;
+  for (int s = 1; s <= kb; ++s) {
+    if (kb % s) continue;
+    if (Kd / s > kLinKcMax) continue;
+    last_ok = s;
+    if (n_tiles * s >= kLinTargetCtas) return s;
+    if (Kd / s <= 2 * kLinBK) return s;  // do not cut a CTA's share below two k blocks
+  }
+  return last_ok;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int n_tiles, int map) {
+  if (!w || !aligned16(w)) return fail(ctx, SV_E_INVAL, "weight pointer null or not 16-byte aligned");
+  d->N = rows;
+  d->Kd = Kd;
+  d->n_tiles = n_tiles;
+  d->splits = choose_splits(n_tiles, Kd);
+  d->Kc = Kd / d->splits;
+  d->map_kind = map;
+  if (!make_map(&d->map, w, (uint64_t)rows, (uint64_t)Kd, 64))
+    return fail(ctx, SV_E_CUDA, "cuTensorMapEncodeTiled failed for a weight of %d x %d", rows, Kd);
+  return SV_OK;
+}
+
+template <typename T>
+int dalloc(sv_ctx* ctx, T** p, size_t count) {
+  void* q = nullptr;
+  size_t bytes = count * sizeof(T);
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) return fail(ctx, SV_E_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  ctx->allocs.push_back(q);
+  *p = static_cast<T*>(q);
+  e = cudaMemset(q, 0, bytes);
+  if (e != cudaSuccess) return fail(ctx, SV_E_CUDA, "cudaMemset failed: %s", cudaGetErrorString(e));
+  return SV_OK;
+}
+
+int mp_of(int M) { return M <= 8 ? 8 : (M <= 16 ? 16 : 32); }
+
+// ------------------------------------------------------------------ the step
+// Enqueue every kernel of one step of M rows on ctx->stream.
+int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
+  const sv_config& c = ctx->cfg;
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  cudaStream_t s = ctx->stream;
+  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, s));
+
+  LinParams base = {};
+  base.ss_tiles = H / 128;
+  base.eps = c.rms_eps;
+  base.M = M;
+  base.ffn = c.ffn;
+  base.head_dim = d;
+  base.ws = ctx->ws;
+  base.counters = ctx->counters;
+  base.block_table = ctx->block_table;
+  base.rope = ctx->rope;
+  base.n_q_heads = Hq;
+  base.n_kv_heads = Hkv;
+  base.act = c.act;
+  base.vocab = c.vocab;
+  base.st = ctx->st;
+
+  AttnParams ap = {};
+  ap.q = ctx->q;
+  ap.block_table = ctx->block_table;
+  ap.st = ctx->st;
+  ap.part_ml = ctx->part_ml;
+  ap.part_o = ctx->part_o;
+  ap.out = ctx->o;
+  ap.M = M;
+  ap.n_q_heads = Hq;
+  ap.n_kv_heads = Hkv;
+  ap.max_splits = ctx->max_splits;
+  ap.max_pages = c.max_pages;
+  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
+  const int G = Hq / Hkv;
+  const int n_rb = (M + kAttnQ / G - 1) / (kAttnQ / G);
+  const int attn_grid = std::max(1, std::min(ctx->max_splits * Hkv * n_rb, ctx->num_sms));
+
+  for (int l = 0; l < c.n_layers; ++l) {
+    const size_t loff = (size_t)l * ctx->layer_stride;
+    {  // RMSNorm + QKV + QK-norm + RoPE + paged K/V write
+      LinParams p = base;
+      const LinearDesc& ld = ctx->lin_qkv[l];
+      p.X = ctx->x;
+      p.x_ss = ctx->x_ss;
+      p.gain = ctx->attn_norm[l];
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.out = ctx->q;
+      p.out_stride = Hq * d;
+      p.kcache = ctx->kpool + loff;
+      p.vcache = ctx->vpool + loff;
+      p.q_gain = c.qk_norm ? ctx->q_norm[l] : nullptr;
+      p.k_gain = c.qk_norm ? ctx->k_norm[l] : nullptr;
+      CK(launch_linear(ld, p, EPI_QKV, true, s, true));
+    }
+    ap.layer = l;
+    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, s, true));
+    CK(launch_attn_combine(ap, d, s, true));
+    {  // attention projection + residual
+      LinParams p = base;
+      const LinearDesc& ld = ctx->lin_o[l];
+      p.X = ctx->o;
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.out = ctx->x;
+      p.out_stride = H;
+      p.out_ss = ctx->x_ss;
+      CK(launch_linear(ld, p, EPI_RESID, false, s, true));
+    }
+    {  // RMSNorm + gate|up + activation
+      LinParams p = base;
+      const LinearDesc& ld = ctx->lin_gu[l];
+      p.X = ctx->x;
+      p.x_ss = ctx->x_ss;
+      p.gain = ctx->ffn_norm[l];
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.out = ctx->a;
+      p.out_stride = c.ffn;
+      CK(launch_linear(ld, p, EPI_GLU, true, s, true));
+    }
+    {  // down projection + residual
+      LinParams p = base;
+      const LinearDesc& ld = ctx->lin_down[l];
+      p.X = ctx->a;
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.out = ctx->x;
+      p.out_stride = H;
+      p.out_ss = ctx->x_ss;
+      CK(launch_linear(ld, p, EPI_RESID, false, s, true));
+    }
+  }
+  if (mode != MODE_BODY) {  // final RMSNorm + LM head + per-tile argmax
+    LinParams p = base;
+    const LinearDesc& ld = ctx->lin_head;
+    p.X = ctx->x;
+    p.x_ss = ctx->x_ss;
+    p.gain = ctx->final_norm;
+    p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+    p.logits = logits;
+    p.logits_row0 = (mode == MODE_PREFILL) ? M - 1 : 0;
+    p.am_val = ctx->am_val;
+    p.am_idx = ctx->am_idx;
+    CK(launch_linear(ld, p, EPI_LOGITS, true, s, true));
+  }
+  CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
+                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s, true));
+  return SV_OK;
+}
+
+// Run one step: replay (capturing on first use) the graph of this shape.
+int run_step(sv_ctx* ctx, int M, int mode, float* logits) {
+  if (!ctx->use_graphs) return enqueue_step(ctx, M, mode, logits);
+  for (auto& g : ctx->graphs)
+    if (g.M == M && g.mode == mode && g.logits == logits) {
+      CK(cudaGraphLaunch(g.exec, ctx->stream));
+      return SV_OK;
+    }
+  if (ctx->graphs.size() >= 64) {
+    for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.exec);
+    ctx->graphs.clear();
+  }
+  CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+  int rc = enqueue_step(ctx, M, mode, logits);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(ctx->stream, &graph);
+  if (rc != SV_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return fail(ctx, SV_E_CUDA, "stream capture failed: %s", cudaGetErrorString(e));
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(ctx, SV_E_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  ctx->graphs.push_back({M, mode, logits, exec});
+  CK(cudaGraphLaunch(exec, ctx->stream));
+  return SV_OK;
+}
+
+// ------------------------------------------------------------------ pages
+int pages_for(int len) { return (len + kPage - 1) / kPage; }
+
+// Give logical pages [n_alloc, pages_for(len)) physical pages and upload them.
+int ensure_pages(sv_ctx* ctx, int len) {
+  const int need = pages_for(len);
+  if (need > ctx->bt_len) return fail(ctx, SV_E_INVAL, "length %d exceeds max_seq %d", len, ctx->cfg.max_seq);
+  if (need <= ctx->n_alloc) return SV_OK;
+  if ((int)ctx->free_pages.size() < need - ctx->n_alloc)
+    return fail(ctx, SV_E_NOMEM, "KV page pool exhausted (%d free, %d needed)",
+                (int)ctx->free_pages.size(), need - ctx->n_alloc);
+  const int first = ctx->n_alloc;
+  for (int lp = first; lp < need; ++lp) {
+    ctx->pin_bt[lp] = ctx->free_pages.back();
+    ctx->free_pages.pop_back();
+  }
+  ctx->n_alloc = need;
+  CK(cudaMemcpyAsync(ctx->block_table + first, ctx->pin_bt + first, (need - first) * sizeof(int),
+                     cudaMemcpyHostToDevice, ctx->stream));
+  return SV_OK;
+}
+
+// Return pages wholly beyond `len` to the pool (their table entries stay
+// stale on the device; cap_len keeps kernels away from them).
+void release_pages(sv_ctx* ctx, int len) {
+  const int keep = pages_for(len);
+  for (int lp = ctx->n_alloc - 1; lp >= keep; --lp) {
+    ctx->free_pages.push_back(ctx->pin_bt[lp]);
+    ctx->pin_bt[lp] = -1;
+  }
+  if (keep < ctx->n_alloc) ctx->n_alloc = keep;
+}
+
+int begin_call(sv_ctx* ctx) {
+  if (ctx->async_pending) return fail(ctx, SV_E_STATE, "asynchronous calls pending: call sv_sync first");
+  CK(cudaEventRecord(ctx->ev, ctx->user_stream));
+  CK(cudaStreamWaitEvent(ctx->stream, ctx->ev, 0));
+  return SV_OK;
+}
+
+int end_call(sv_ctx* ctx) {
+  CK(cudaEventRecord(ctx->ev, ctx->stream));
+  CK(cudaStreamWaitEvent(ctx->user_stream, ctx->ev, 0));
+  return SV_OK;
+}
+
+// Stage [cap_len, tokens[0..n)] at slot `at` of the pinned input buffer and
+// copy it into the device state.
+int upload_tokens(sv_ctx* ctx, const int32_t* tokens, int n, int at) {
+  int32_t* src = ctx->pin_in + at;
+  src[0] = ctx->n_alloc * kPage;
+  memcpy(src + 1, tokens, n * sizeof(int32_t));
+  CK(cudaMemcpyAsync(&ctx->st->cap_len, src, (n + 1) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                     ctx->stream));
+  return SV_OK;
+}
+
+int check_tokens(sv_ctx* ctx, const int32_t* t, int n) {
+  if (!t) return fail(ctx, SV_E_INVAL, "token array is null");
+  for (int i = 0; i < n; ++i)
+    if (t[i] < 0 || t[i] >= ctx->cfg.vocab)
+      return fail(ctx, SV_E_INVAL, "token %d out of range [0, %d)", t[i], ctx->cfg.vocab);
+  return SV_OK;
+}
+
+int finish_sync_step(sv_ctx* ctx, int32_t* result) {
+  CK(cudaMemcpyAsync(ctx->pin_out, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                     ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  memcpy(result, ctx->pin_out, 4 * sizeof(int32_t));
+  if (result[3] != 0)
+    return fail(ctx, SV_E_CUDA, "a kernel reported status 0x%x (1 timeout, 2 bad page, 4 bad token)",
+                result[3]);
+  ctx->seq_len = result[2];
+  release_pages(ctx, ctx->seq_len);
+  return SV_OK;
+}
+
+int validate(const sv_config* c) {
+  if (!c) return 0;
+  if (c->n_layers < 0 || c->hidden <= 0 || c->hidden % 128) return 0;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return 0;
+  if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads) return 0;
+  if (16 % (c->n_q_heads / c->n_kv_heads)) return 0;
+  if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % 128) return 0;
+  if ((c->n_q_heads * c->head_dim) % 64) return 0;
+  if (c->ffn <= 0 || c->ffn % 64) return 0;
+  if (c->vocab <= 0) return 0;
+  if (c->qk_norm && c->head_dim > 128) return 0;
+  if (c->act != 0 && c->act != 1) return 0;
+  if (c->page_size != kPage || c->max_k < 1 || c->max_k > kMaxK) return 0;
+  if (c->max_seq < c->max_k || c->max_pages < 1) return 0;
+  return 1;
+}
+
+}  // namespace
+
+// ====================================================================== API
+extern "C" {
+
+int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_ctx** out) {
+  if (!out) return SV_E_INVAL;
+  *out = nullptr;
+  if (!validate(cfg) || !w) return SV_E_INVAL;
+  sv_ctx* ctx = new sv_ctx();
+  ctx->cfg = *cfg;
+  const sv_config& c = ctx->cfg;
+  int rc = SV_OK;
+  auto bail = [&](int code) {
+    sv_destroy(ctx);
+    return code;
+  };
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) return bail(SV_E_CUDA);
+  cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (ctx->num_sms <= 0) ctx->num_sms = 1;
+  ctx->user_stream = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(SV_E_CUDA);
+  if (cudaEventCreateWithFlags(&ctx->ev, cudaEventDisableTiming) != cudaSuccess) return bail(SV_E_CUDA);
+  const char* ng = getenv("SV_NO_GRAPHS");
+  ctx->use_graphs = !(ng && ng[0] == '1');
+  if (prepare_linear_kernels() != cudaSuccess || prepare_attention_kernels() != cudaSuccess)
+    return bail(SV_E_CUDA);
+
+  const int L = c.n_layers, H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  ctx->embed = static_cast<const bf16*>(w->embed);
+  ctx->lm_head = static_cast<const bf16*>(w->lm_head ? w->lm_head : w->embed);
+  ctx->final_norm = static_cast<const bf16*>(w->final_norm);
+  if (!ctx->embed || !ctx->final_norm || !aligned16(ctx->final_norm)) return bail(SV_E_INVAL);
+  if (L > 0 && (!w->attn_norm || !w->wqkv || !w->wo || !w->ffn_norm || !w->w_gate_up || !w->w_down ||
+                (c.qk_norm && (!w->q_norm || !w->k_norm))))
+    return bail(SV_E_INVAL);
+  ctx->lin_qkv.resize(L);
+  ctx->lin_o.resize(L);
+  ctx->lin_gu.resize(L);
+  ctx->lin_down.resize(L);
+  const int qkv_rows = (Hq + 2 * Hkv) * d;
+  for (int l = 0; l < L; ++l) {
+    ctx->attn_norm.push_back(static_cast<const bf16*>(w->attn_norm[l]));
+    ctx->ffn_norm.push_back(static_cast<const bf16*>(w->ffn_norm[l]));
+    ctx->q_norm.push_back(c.qk_norm ? static_cast<const bf16*>(w->q_norm[l]) : nullptr);
+    ctx->k_norm.push_back(c.qk_norm ? static_cast<const bf16*>(w->k_norm[l]) : nullptr);
+    if (!aligned16(w->attn_norm[l]) || !aligned16(w->ffn_norm[l]) || !w->attn_norm[l] || !w->ffn_norm[l])
+      return bail(SV_E_INVAL);
+    if ((rc = make_linear(ctx, &ctx->lin_qkv[l], w->wqkv[l], qkv_rows, H, qkv_rows / 128,
+                          d == 256 ? MAP_HEAD256 : MAP_PLAIN)))
+      return bail(rc);
+    if ((rc = make_linear(ctx, &ctx->lin_o[l], w->wo[l], H, Hq * d, H / 128, MAP_PLAIN))) return bail(rc);
+    if ((rc = make_linear(ctx, &ctx->lin_gu[l], w->w_gate_up[l], 2 * c.ffn, H, c.ffn / 64, MAP_GATE_UP)))
+      return bail(rc);
+    if ((rc = make_linear(ctx, &ctx->lin_down[l], w->w_down[l], H, c.ffn, H / 128, MAP_PLAIN)))
+      return bail(rc);
+  }
+  if ((rc = make_linear(ctx, &ctx->lin_head, ctx->lm_head, c.vocab, H, (c.vocab + 127) / 128, MAP_PLAIN)))
+    return bail(rc);
+
+  // ---- device memory
+  const int MP = mp_of(c.max_k);
+  ctx->bt_len = pages_for(c.max_seq);
+  ctx->layer_stride = (size_t)c.max_pages * Hkv * kPage * d;
+  const size_t pool = ctx->layer_stride * (L > 0 ? L : 1);
+  ctx->max_splits = (c.max_seq + kAttnSplit - 1) / kAttnSplit;
+  size_t ws_floats = 0;
+  int max_tiles = ctx->lin_head.n_tiles;
+  auto acc_ws = [&](const LinearDesc& ld) {
+    if (ld.splits > 1) ws_floats = std::max(ws_floats, (size_t)ld.n_tiles * ld.splits * kLinRows * MP);
+    max_tiles = std::max(max_tiles, ld.n_tiles);
+  };
+  for (int l = 0; l < L; ++l) {
+    acc_ws(ctx->lin_qkv[l]);
+    acc_ws(ctx->lin_o[l]);
+    acc_ws(ctx->lin_gu[l]);
+    acc_ws(ctx->lin_down[l]);
+  }
+  acc_ws(ctx->lin_head);
+  if ((rc = dalloc(ctx, &ctx->kpool, pool)) || (rc = dalloc(ctx, &ctx->vpool, pool)) ||
+      (rc = dalloc(ctx, &ctx->block_table, (size_t)ctx->bt_len)) || (rc = dalloc(ctx, &ctx->st, 1)) ||
+      (rc = dalloc(ctx, &ctx->x, (size_t)kMaxK * H)) ||
+      (rc = dalloc(ctx, &ctx->q, (size_t)kMaxK * Hq * d)) ||
+      (rc = dalloc(ctx, &ctx->o, (size_t)kMaxK * Hq * d)) ||
+      (rc = dalloc(ctx, &ctx->a, (size_t)kMaxK * c.ffn)) ||
+      (rc = dalloc(ctx, &ctx->x_ss, (size_t)kMaxK * (H / 128))) ||
+      (rc = dalloc(ctx, &ctx->rope, (size_t)c.max_seq * (d / 2))) ||
+      (rc = dalloc(ctx, &ctx->part_ml, (size_t)c.max_k * Hq * ctx->max_splits)) ||
+      (rc = dalloc(ctx, &ctx->part_o, (size_t)c.max_k * Hq * ctx->max_splits * d)) ||
+      (rc = dalloc(ctx, &ctx->ws, ws_floats)) || (rc = dalloc(ctx, &ctx->counters, (size_t)max_tiles)) ||
+      (rc = dalloc(ctx, &ctx->am_val, (size_t)kMaxK * ctx->lin_head.n_tiles)) ||
+      (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
+    return bail(rc);
+  if (!make_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
+      !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage))
+    return bail(SV_E_CUDA);
+  if (cudaMallocHost(&ctx->pin_in, sizeof(int32_t) * ((size_t)c.max_seq + 2 * kMaxK + 8)) != cudaSuccess ||
+      cudaMallocHost(&ctx->pin_out, sizeof(int32_t) * 8) != cudaSuccess ||
+      cudaMallocHost(&ctx->pin_bt, sizeof(int) * (size_t)ctx->bt_len) != cudaSuccess)
+    return bail(SV_E_NOMEM);
+  for (int i = 0; i < ctx->bt_len; ++i) ctx->pin_bt[i] = -1;
+  if (cudaMemcpy(ctx->block_table, ctx->pin_bt, sizeof(int) * ctx->bt_len, cudaMemcpyHostToDevice) !=
+      cudaSuccess)
+    return bail(SV_E_CUDA);
+  for (int pg = c.max_pages - 1; pg >= 0; --pg) ctx->free_pages.push_back(pg);
+  if (launch_rope_table(ctx->rope, c.max_seq, d, c.rope_theta, ctx->stream) != cudaSuccess ||
+      cudaStreamSynchronize(ctx->stream) != cudaSuccess)
+    return bail(SV_E_CUDA);
+  *out = ctx;
+  return SV_OK;
+}
+
+void sv_destroy(sv_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+  for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.exec);
+  for (void* p : ctx->allocs) cudaFree(p);
+  if (ctx->pin_in) cudaFreeHost(ctx->pin_in);
+  if (ctx->pin_out) cudaFreeHost(ctx->pin_out);
+  if (ctx->pin_bt) cudaFreeHost(ctx->pin_bt);
+  if (ctx->ev) cudaEventDestroy(ctx->ev);
+  if (ctx->stream) cudaStreamDestroy(ctx->stream);
+  delete ctx;
+}
+
+int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev, int32_t* n_accepted,
+              int32_t* correction_token) {
+  if (!ctx) return SV_E_INVAL;
+  if (K < 1 || K > ctx->cfg.max_k) return fail(ctx, SV_E_INVAL, "K=%d outside [1, %d]", K, ctx->cfg.max_k);
+  int rc;
+  if ((rc = check_tokens(ctx, tokens_host, K))) return rc;
+  if (ctx->seq_len + K > ctx->cfg.max_seq)
+    return fail(ctx, SV_E_INVAL, "length %d + %d exceeds max_seq", ctx->seq_len, K);
+  if ((rc = begin_call(ctx))) return rc;
+  if ((rc = ensure_pages(ctx, ctx->seq_len + K))) return rc;
+  if ((rc = upload_tokens(ctx, tokens_host, K, 0))) return rc;
+  if ((rc = run_step(ctx, K, MODE_VERIFY, logits_dev))) return rc;
+  int32_t res[4];
+  if ((rc = finish_sync_step(ctx, res))) return rc;
+  if (n_accepted) *n_accepted = res[0];
+  if (correction_token) *correction_token = res[1];
+  return end_call(ctx);
+}
+
+int sv_decode(sv_ctx* ctx, int32_t token, float* logits_dev, int32_t* next_token) {
+  int32_t n = 0;
+  return sv_verify(ctx, &token, 1, logits_dev, &n, next_token);
+}
+
+int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logits_dev,
+               int32_t* next_token) {
+  if (!ctx) return SV_E_INVAL;
+  if (n < 1) return fail(ctx, SV_E_INVAL, "prefill of %d tokens", n);
+  int rc;
+  if ((rc = check_tokens(ctx, tokens_host, n))) return rc;
+  if (ctx->seq_len + n > ctx->cfg.max_seq)
+    return fail(ctx, SV_E_INVAL, "length %d + %d exceeds max_seq", ctx->seq_len, n);
+  if ((rc = begin_call(ctx))) return rc;
+  if ((rc = ensure_pages(ctx, ctx->seq_len + n))) return rc;
+  const int B = ctx->cfg.max_k;
+  int at = 0;
+  for (int done = 0; done < n; done += B) {
+    const int M = std::min(B, n - done);
+    const bool last = done + M == n;
+    if ((rc = upload_tokens(ctx, tokens_host + done, M, at))) return rc;
+    at += M + 1;
+    if ((rc = run_step(ctx, M, last ? MODE_PREFILL : MODE_BODY, last ? last_logits_dev : nullptr)))
+      return rc;
+  }
+  int32_t res[4];
+  if ((rc = finish_sync_step(ctx, res))) return rc;
+  if (next_token) *next_token = res[1];
+  return end_call(ctx);
+}
+
+int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits_dev, int32_t* result_dev) {
+  if (!ctx) return SV_E_INVAL;
+  if (K < 1 || K > ctx->cfg.max_k) return fail(ctx, SV_E_INVAL, "K=%d outside [1, %d]", K, ctx->cfg.max_k);
+  if (!tokens_dev || !result_dev) return fail(ctx, SV_E_INVAL, "null device pointer");
+  if (!ctx->async_pending) {
+    CK(cudaEventRecord(ctx->ev, ctx->user_stream));
+    CK(cudaStreamWaitEvent(ctx->stream, ctx->ev, 0));
+  }
+  ctx->async_pending = true;
+  CK(cudaMemcpyAsync(ctx->st->tokens, tokens_dev, K * sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
+  int rc = run_step(ctx, K, MODE_VERIFY, logits_dev);
+  if (rc) return rc;
+  CK(cudaMemcpyAsync(result_dev, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
+  CK(cudaEventRecord(ctx->ev, ctx->stream));
+  CK(cudaStreamWaitEvent(ctx->user_stream, ctx->ev, 0));
+  return SV_OK;
+}
+
+int sv_reserve(sv_ctx* ctx, int len) {
+  if (!ctx) return SV_E_INVAL;
+  if (len < 0 || len > ctx->cfg.max_seq) return fail(ctx, SV_E_INVAL, "reserve %d outside [0, max_seq]", len);
+  int rc;
+  if ((rc = begin_call(ctx))) return rc;
+  if ((rc = ensure_pages(ctx, len))) return rc;
+  CK(launch_set_len(ctx->st, ctx->seq_len, ctx->n_alloc * kPage, ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  return end_call(ctx);
+}
+
+int sv_sync(sv_ctx* ctx) {
+  if (!ctx) return SV_E_INVAL;
+  CK(cudaStreamSynchronize(ctx->stream));
+  CK(cudaMemcpy(ctx->pin_out, ctx->st, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  ctx->async_pending = false;
+  ctx->seq_len = ctx->pin_out[0];
+  if (ctx->pin_out[2] != 0)
+    return fail(ctx, SV_E_CUDA, "a kernel reported status 0x%x (1 timeout, 2 bad page, 4 bad token)",
+                ctx->pin_out[2]);
+  return SV_OK;
+}
+
+int sv_truncate(sv_ctx* ctx, int new_len) {
+  if (!ctx) return SV_E_INVAL;
+  if (new_len < 0 || new_len > ctx->seq_len)
+    return fail(ctx, SV_E_INVAL, "truncate to %d outside [0, %d]", new_len, ctx->seq_len);
+  int rc;
+  if ((rc = begin_call(ctx))) return rc;
+  const sv_config& c = ctx->cfg;
+  CK(launch_kv_zero(ctx->kpool, ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers,
+                    c.n_kv_heads, c.head_dim, new_len, ctx->seq_len, ctx->stream));
+  ctx->seq_len = new_len;
+  release_pages(ctx, new_len);
+  CK(launch_set_len(ctx->st, new_len, ctx->n_alloc * kPage, ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  return end_call(ctx);
+}
+
+int sv_seq_len(const sv_ctx* ctx) { return ctx ? ctx->seq_len : SV_E_INVAL; }
+
+int sv_kv_read(sv_ctx* ctx, int layer, int first, int count, void* k_dst_dev, void* v_dst_dev) {
+  if (!ctx) return SV_E_INVAL;
+  const sv_config& c = ctx->cfg;
+  if (layer < 0 || layer >= c.n_layers || first < 0 || count < 0 || first + count > ctx->seq_len ||
+      !k_dst_dev || !v_dst_dev)
+    return fail(ctx, SV_E_INVAL, "kv_read(layer %d, %d, %d) outside the sequence", layer, first, count);
+  int rc;
+  if ((rc = begin_call(ctx))) return rc;
+  CK(launch_kv_gather(ctx->kpool, ctx->vpool, ctx->layer_stride, ctx->block_table, layer, c.n_kv_heads,
+                      c.head_dim, first, count, static_cast<bf16*>(k_dst_dev), static_cast<bf16*>(v_dst_dev),
+                      ctx->stream));
+  CK(cudaStreamSynchronize(ctx->stream));
+  return end_call(ctx);
+}
+
+int sv_shuffle_pages(sv_ctx* ctx, uint64_t seed) {
+  if (!ctx) return SV_E_INVAL;
+  uint64_t z = seed;
+  auto next = [&z]() {  // splitmix64 step
+    z += 0x9E3779B97F4A7C15ull;
+    uint64_t r = z;
+    r = (r ^ (r >> 30)) * 0xBF58476D1CE4E5B9ull;
+    r = (r ^ (r >> 27)) * 0x94D049BB133111EBull;
+    return r ^ (r >> 31);
+  };
+  auto& f = ctx->free_pages;
+  for (size_t i = f.size(); i > 1; --i) std::swap(f[i - 1], f[next() % i]);
+  return SV_OK;
+}
+
+int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head) {
+  if (!ctx || K < 1) return SV_E_INVAL;
+  return 1 + 6 * ctx->cfg.n_layers + (with_head ? 2 : 1);
+}
+
+int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, double* bytes_per_launch) {
+  if (!ctx) return SV_E_INVAL;
+  const sv_config& c = ctx->cfg;
+  if (which < SV_LIN_O || which > SV_LIN_LM_HEAD || K < 1 || K > c.max_k || reps < 1 || !avg_us)
+    return fail(ctx, SV_E_INVAL, "sv_time_linear(which=%d, K=%d, reps=%d)", which, K, reps);
+  if (which != SV_LIN_LM_HEAD && c.n_layers < 1) return fail(ctx, SV_E_INVAL, "model has no layers");
+  int rc;
+  if ((rc = begin_call(ctx))) return rc;
+  const int H = c.hidden;
+  LinParams base = {};
+  base.ss_tiles = H / 128;
+  base.eps = c.rms_eps;
+  base.M = K;
+  base.ffn = c.ffn;
+  base.head_dim = c.head_dim;
+  base.ws = ctx->ws;
+  base.counters = ctx->counters;
+  base.n_q_heads = c.n_q_heads;
+  base.n_kv_heads = c.n_kv_heads;
+  base.act = c.act;
+  base.vocab = c.vocab;
+  base.st = ctx->st;
+  base.x_ss = ctx->x_ss;
+  base.am_val = ctx->am_val;
+  base.am_idx = ctx->am_idx;
+  // one launch per layer (distinct weights, so nothing is served from L2),
+  // chained with programmatic dependent launch as inside a step
+  const int per = (which == SV_LIN_LM_HEAD) ? 1 : c.n_layers;
+  cudaEvent_t e0, e1;
+  CK(cudaEventCreate(&e0));
+  CK(cudaEventCreate(&e1));
+  double bytes = 0.0;
+  for (int r = -1; r < reps; ++r) {  // r = -1: untimed warm-up pass
+    if (r == 0) CK(cudaEventRecord(e0, ctx->stream));
+    for (int l = 0; l < per; ++l) {
+      LinParams p = base;
+      const LinearDesc* ld;
+      int epi;
+      bool norm;
+      if (which == SV_LIN_O) {
+        ld = &ctx->lin_o[l]; epi = EPI_RESID; norm = false; p.X = ctx->o; p.out = ctx->x; p.out_stride = H;
+        p.out_ss = ctx->x_ss;
+      } else if (which == SV_LIN_GATE_UP) {
+        ld = &ctx->lin_gu[l]; epi = EPI_GLU; norm = true; p.X = ctx->x; p.gain = ctx->ffn_norm[l];
+        p.out = ctx->a; p.out_stride = c.ffn;
+      } else if (which == SV_LIN_DOWN) {
+        ld = &ctx->lin_down[l]; epi = EPI_RESID; norm = false; p.X = ctx->a; p.out = ctx->x; p.out_stride = H;
+        p.out_ss = ctx->x_ss;
+      } else {
+        ld = &ctx->lin_head; epi = EPI_LOGITS; norm = true; p.X = ctx->x; p.gain = ctx->final_norm;
+      }
+      p.Kd = ld->Kd; p.n_tiles = ld->n_tiles; p.splits = ld->splits; p.Kc = ld->Kc; p.map = ld->map_kind;
+      CK(launch_linear(*ld, p, epi, norm, ctx->stream, !(r == 0 && l == 0)));
+      if (r == 0) {
+        const double n_out = which == SV_LIN_GATE_UP ? (double)c.ffn : (double)ld->N;
+        bytes += 2.0 * ld->N * ld->Kd + 2.0 * K * ld->Kd + 2.0 * K * n_out;
+      }
+    }
+  }
+  CK(cudaEventRecord(e1, ctx->stream));
+  CK(cudaEventSynchronize(e1));
+  float ms = 0.0f;
+  CK(cudaEventElapsedTime(&ms, e0, e1));
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  *avg_us = 1000.0f * ms / (float)(reps * per);
+  if (bytes_per_launch) *bytes_per_launch = bytes / per;
+  return end_call(ctx);
+}
+
+const char* sv_last_error(const sv_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+// sv_internal.h -- shared declarations of the sv library's kernels and host code.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sv.h"
+
+namespace sv {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kPage = SV_PAGE_SIZE;
+constexpr int kMaxK = SV_MAX_K;
+
+// Linear kernel geometry: a tile is 128 output rows (two 64-row chunks that
+// TMA loads as separate 64x64 boxes), streamed in 64-column k blocks.
+constexpr int kLinRows = 128;
+constexpr int kLinBK = 64;
+constexpr int kLinChunkBytes = 64 * 128;           // one 64 x 64 bf16 box, 128B-swizzled
+constexpr int kLinStageBytes = 2 * kLinChunkBytes;  // both chunks of one k block
+constexpr int kLinStages = 4;
+constexpr int kLinConsumerWarps = 8;
+constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;
+constexpr int kLinKcMax = 1024;  // most input columns one CTA stages (bounds its smem)
+constexpr int kLinTargetCtas = 304;
+
+// Attention geometry: a split is 256 absolute positions = 4 warps x 4 pages.
+constexpr int kAttnWarps = 4;
+constexpr int kAttnPagesPerWarp = 4;
+constexpr int kAttnSplit = kAttnWarps * kAttnPagesPerWarp * kPage;  // 256
+constexpr int kAttnQ = 16;  // query rows (token rows x heads of one group) per work item
+
+// Kinds of linear epilogue.
+enum LinEpi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_GLU = 2, EPI_LOGITS = 3 };
+// How a tile index maps to its two 64-row chunks of the weight matrix.
+enum LinMap : int { MAP_PLAIN = 0, MAP_GATE_UP = 1, MAP_HEAD256 = 2 };
+// Step kinds.
+enum StepMode : int { MODE_VERIFY = 0, MODE_PREFILL = 1, MODE_BODY = 2 };
+// Status bits a kernel can raise.
+enum Status : int { ST_TIMEOUT = 1, ST_BAD_PAGE = 2, ST_BAD_TOKEN = 4 };
+
+// Device-resident state of the sequence and of the current step.
+// cap_len and tokens are adjacent so the host sets both with one copy.
+struct SvState {
+  int32_t seq_len;   // committed length
+  int32_t step_pos;  // length when the current step started
+  int32_t status;    // Status bits raised so far (sticky)
+  int32_t cap_len;   // positions < cap_len have pages
+  int32_t tokens[kMaxK];
+  int32_t result[4];  // n_accepted, correction, new_len, status
+  int32_t argmax[kMaxK];
+};
+
+struct LinParams {
+  // input activations [M, Kd] bf16 and, for an RMSNorm prologue, the
+  // per-128-column partial sums of squares of each row and the gain
+  const bf16* X;
+  const float* x_ss;  // [kMaxK, ss_tiles]
+  const bf16* gain;   // [Kd]
+  int ss_tiles;
+  float eps;
+  int M, Kd, n_tiles, splits, Kc, map, ffn, head_dim;
+  float* ws;     // split-K partial tiles
+  int* counters; // one ticket per tile
+  // epilogue operands
+  bf16* out;           // EPI_QKV: q [M, Hq d]; EPI_RESID: x [M, N] (in place); EPI_GLU: a [M, ffn]
+  int out_stride;
+  float* out_ss;       // EPI_RESID: [kMaxK, n_tiles] partial sums of squares of the new rows
+  bf16* kcache;        // EPI_QKV: this layer's K pages [pages, Hkv, 16, d]
+  bf16* vcache;
+  const int* block_table;
+  const float2* rope;  // [max_seq, d/2] (cos, sin)
+  const bf16* q_gain;  // [d] or null
+  const bf16* k_gain;
+  int n_q_heads, n_kv_heads, act;
+  float* logits;       // EPI_LOGITS: rows m >= logits_row0 go to logits[m - logits_row0, :]
+  int logits_row0;
+  float* am_val;       // [kMaxK, n_tiles]
+  int* am_idx;
+  int vocab;
+  SvState* st;
+};
+
+struct AttnParams {
+  const bf16* q;  // [M, Hq d]
+  const int* block_table;
+  SvState* st;
+  float2* part_ml;  // [kMaxK, Hq, max_splits] (running max in log2 units, sum)
+  float* part_o;    // [kMaxK, Hq, max_splits, d]
+  bf16* out;        // [M, Hq d]
+  int M, n_q_heads, n_kv_heads, max_splits;
+  int layer, max_pages;  // row coordinate of a page in the pool's tensor maps
+  float scale_log2;      // log2(e) / sqrt(d)
+};
+
+// ------------------------------------------------------------------ launches
+struct LinearDesc {
+  CUtensorMap map;
+  int N, Kd, n_tiles, splits, Kc, map_kind;
+};
+
+cudaError_t prepare_linear_kernels();
+cudaError_t prepare_attention_kernels();
+cudaError_t launch_linear(const LinearDesc& d, const LinParams& p, int epi, bool norm,
+                          cudaStream_t s, bool pdl);
+size_t linear_smem_bytes(int mt, int Kc);
+cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
+                             int head_dim, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_attn_combine(const AttnParams& p, int head_dim, cudaStream_t s, bool pdl);
+cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
+                         SvState* st, cudaStream_t s);
+cudaError_t launch_accept(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
+                          int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
+                          const int* block_table, int n_layers, int n_kv_heads, int head_dim,
+                          cudaStream_t s, bool pdl);
+cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, float theta, cudaStream_t s);
+cudaError_t launch_kv_zero(bf16* kpool, bf16* vpool, size_t layer_stride, const int* block_table,
+                           int n_layers, int n_kv_heads, int head_dim, int first, int last,
+                           cudaStream_t s);
+cudaError_t launch_kv_gather(const bf16* kpool, const bf16* vpool, size_t layer_stride,
+                             const int* block_table, int layer, int n_kv_heads, int head_dim,
+                             int first, int count, bf16* kdst, bf16* vdst, cudaStream_t s);
+cudaError_t launch_set_len(SvState* st, int len, int cap_len, cudaStream_t s);
+
+}  // namespace sv

@@ -1,0 +1,174 @@
+/* sv.h -- batch-invariant block verify for greedy speculative decoding (sm_103a).
+ *
+ * One context holds one sequence of a decoder-only transformer whose weights
+ * live in device memory.  Its committed prefix is kept in a paged K/V cache
+ * (page size 16, block table, pages from a fixed pool).  Every call runs the
+ * same hand-written CUDA kernels on the context's stream:
+ *   embed -> per layer [RMSNorm+QKV linear with QK-norm, RoPE and paged K/V
+ *   write fused in its epilogue; split-KV paged attention (row r of a call sees
+ *   pos+r+1 positions); attention projection + residual; RMSNorm+gate|up
+ *   linear with SwiGLU/GeGLU; down projection + residual] -> final RMSNorm +
+ *   LM head with per-tile argmax -> argmax/accept/truncate.
+ *
+ * Verify semantics follow "Phase 23: Speculative Verify Parity" section 2:
+ * write the window's K/V into the committed cache in one shot (step 1), give
+ * each row its own context length (step 2), compute rows with the same
+ * rounding path as single-token decode (step 3), keep the K/V on acceptance
+ * (step 4), truncate to the accepted prefix on rejection (step 5).  The
+ * acceptance rule is the greedy one of "Shape and cache history in Gemma block
+ * verification", section "Mechanism and failure": a draft is kept only while it
+ * equals the target's greedy token after the same preceding ids; the
+ * correction token is the target's greedy token at the first mismatch.
+ *
+ * Batch invariance: row r of any call is bit-identical to a single-token
+ * decode at the same prefix, and results do not depend on how the cache was
+ * built (one-token commits, block commits, one prefill) or on which physical
+ * pages hold it.  Logits are returned as fp32 holding bf16 values; argmax ties
+ * go to the lowest token id.
+ *
+ * Conventions for every call:
+ *   - Return 0 (SV_OK) or a negative SV_E_* code; sv_last_error() then gives a
+ *     message.  On SV_E_INVAL / SV_E_NOMEM the sequence state is unchanged.
+ *     SV_E_CUDA means a CUDA call or a kernel's own bounds/timeout check
+ *     failed; the context should then be destroyed.
+ *   - Host pointers are read or written before the call returns; device
+ *     pointers must stay valid until the work on the context's stream is done.
+ *   - Calls on one context must not overlap (one host thread at a time).
+ */
+#ifndef SV_H
+#define SV_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SV_OK 0
+#define SV_E_INVAL (-1)       /* bad argument or unsupported shape */
+#define SV_E_NOMEM (-2)       /* page pool or device memory exhausted */
+#define SV_E_CUDA (-3)        /* CUDA error or a kernel reported a failed check */
+#define SV_E_STATE (-4)       /* call not valid in the current state */
+
+#define SV_PAGE_SIZE 16       /* positions per KV page */
+#define SV_MAX_K 32           /* most rows in one verify / prefill block */
+
+typedef struct sv_ctx sv_ctx;
+
+/* Model shape and context limits.
+ *   hidden % 128 == 0; ffn % 64 == 0; (n_q_heads + 2 n_kv_heads) head_dim % 128
+ *   == 0; head_dim in {64, 128, 256}; qk_norm requires head_dim <= 128;
+ *   n_q_heads % n_kv_heads == 0 and 16 % (n_q_heads / n_kv_heads) == 0.
+ *   act: 0 = SwiGLU silu(gate)*up, 1 = GeGLU with tanh-approximated GELU.
+ *   page_size must be 16.  max_k in [1, 32].  max_seq: longest sequence
+ *   (committed + window); max_pages: KV pool size in pages (>= max_seq/16 for
+ *   one full sequence). */
+typedef struct {
+  int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+  float rms_eps, rope_theta;
+  int32_t qk_norm, act, tie_embeddings;
+  int32_t page_size, max_pages, max_k, max_seq;
+} sv_config;
+
+/* Device pointers to bf16 weights, row-major, borrowed for the context's
+ * lifetime (the caller keeps them allocated and unchanged).  Each must be
+ * 16-byte aligned.  Per-layer fields are HOST arrays of n_layers device
+ * pointers (read during sv_create only).
+ *   embed, lm_head [vocab, hidden] (lm_head may equal embed); final_norm [hidden]
+ *   attn_norm, ffn_norm [hidden]; q_norm, k_norm [head_dim] (ignored if !qk_norm)
+ *   wqkv [(n_q_heads + 2 n_kv_heads) head_dim, hidden]: q heads, k heads, v heads
+ *   wo [hidden, n_q_heads head_dim]
+ *   w_gate_up [2 ffn, hidden]: gate rows then up rows
+ *   w_down [hidden, ffn]                                                        */
+typedef struct {
+  const void *embed, *lm_head, *final_norm;
+  const void *const *attn_norm, *const *wqkv, *const *q_norm, *const *k_norm;
+  const void *const *wo, *const *ffn_norm, *const *w_gate_up, *const *w_down;
+} sv_weights;
+
+/* Create a context on the current CUDA device.  cuda_stream: the caller's
+ * stream (cudaStream_t) or NULL for the legacy stream; the library orders its
+ * own internal stream after it at the start of each call and the caller's
+ * stream after the library's work at the end.  Allocates the KV pool, block
+ * table, activations and workspaces (all owned by the context). */
+int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_ctx** out);
+void sv_destroy(sv_ctx* ctx);
+
+/* Commit n tokens (host array) at positions len .. len+n-1, processed in
+ * row blocks of at most max_k rows.  last_logits_dev: device fp32 [vocab] for
+ * the logits after the last token, or NULL.  next_token: the greedy token
+ * after the last one.  Synchronous. */
+int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logits_dev,
+               int32_t* next_token);
+
+/* Commit one token and return the greedy next token; logits_dev [vocab] or
+ * NULL.  Identical to sv_verify with K = 1.  Synchronous. */
+int sv_decode(sv_ctx* ctx, int32_t token, float* logits_dev, int32_t* next_token);
+
+/* Block verify of K rows (host array) [pending, d_1 .. d_{K-1}] at positions
+ * pos .. pos+K-1 (pos = current length).  Row 0 is always committed; drafts
+ * are accepted while d_{j+1} equals the argmax of row j.  On return
+ * n_accepted in [0, K-1], correction_token = argmax of row n_accepted, the
+ * length is pos + 1 + n_accepted, and the K/V of rejected rows are zeroed.
+ * logits_dev: device fp32 [K, vocab] or NULL.  Synchronous. */
+int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev,
+              int32_t* n_accepted, int32_t* correction_token);
+
+/* Asynchronous verify with device-resident input and output, for callers that
+ * keep drafts on the GPU.  tokens_dev: int32 [K]; result_dev: int32 [4] =
+ * {n_accepted, correction_token, new_length, status (0 = ok)}.  The sequence
+ * length is tracked on the device; pages must already cover every position
+ * the call writes (see sv_reserve), otherwise the kernels skip the writes and
+ * report a nonzero status.  Call sv_sync before any synchronous call. */
+int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits_dev,
+                    int32_t* result_dev);
+
+/* Make pages cover positions [0, len).  Synchronous. */
+int sv_reserve(sv_ctx* ctx, int len);
+
+/* Wait for asynchronous calls, read the device length back, release pages
+ * beyond it, and report any kernel status error.  */
+int sv_sync(sv_ctx* ctx);
+
+/* Roll the sequence back to new_len <= length: zero the K/V of the removed
+ * positions and release their pages.  Synchronous. */
+int sv_truncate(sv_ctx* ctx, int new_len);
+
+/* Current committed length (as of the last synchronous call or sv_sync). */
+int sv_seq_len(const sv_ctx* ctx);
+
+/* Copy the cached K and V of positions [first, first+count) of one layer into
+ * device buffers k_dst_dev, v_dst_dev, each bf16 [count, n_kv_heads, head_dim].
+ * Positions must be < length.  Synchronous. */
+int sv_kv_read(sv_ctx* ctx, int layer, int first, int count, void* k_dst_dev, void* v_dst_dev);
+
+/* Shuffle the order in which free pages are handed out (seeded).  Results
+ * must not depend on it; tests use it to build the same prefix on different
+ * physical pages. */
+int sv_shuffle_pages(sv_ctx* ctx, uint64_t seed);
+
+/* Number of kernel launches in one step of K rows, with (1) or without (0)
+ * the LM head and acceptance. */
+int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head);
+
+/* Measurement hook for the dominant kernel class.  Launches one linear of the
+ * model for K rows, once per layer (distinct weights, so every launch streams
+ * from HBM), `reps` times after one untimed pass, chained as inside a step on
+ * the context's stream, and timed with CUDA events on that stream.
+ *   which: SV_LIN_O, SV_LIN_GATE_UP, SV_LIN_DOWN or SV_LIN_LM_HEAD
+ *   avg_us: mean device time per launch
+ *   bytes_per_launch (or NULL): algorithmic bytes of one launch = weight bytes
+ *     + input rows + output rows (bf16)
+ * Overwrites the step's scratch activations; the sequence and its cache are
+ * untouched.  Synchronous. */
+#define SV_LIN_O 1
+#define SV_LIN_GATE_UP 2
+#define SV_LIN_DOWN 3
+#define SV_LIN_LM_HEAD 4
+int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, double* bytes_per_launch);
+
+const char* sv_last_error(const sv_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -275,3 +275,28 @@ def schedule(chain: list[int], K: int, n_steps: int, **kw):
         out.append((i, toks, n))
         i += n + 1
     return out
+
+
+# ------------------------------------------------------------ device copies
+def device_weights(cfg: ModelConfig, seed: int = 0, gain_std: float = 0.0, host: HostWeights = None,
+                   device: str = "cuda"):
+    """Weights as CUDA bf16 tensors keyed (name, layer): copied from ``host``
+    when given, else generated in device memory by the device implementation of
+    the same generator (bit-identical by construction)."""
+    import torch
+    out = {}
+    for key, layer, tid, shape, kind in tensor_specs(cfg):
+        if host is not None:
+            a = host.tensors[(key, layer)]
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+            out[(key, layer)] = t.to(device)
+        else:
+            t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+            if kind == "w":
+                device_fill(t.data_ptr(), t.numel(), seed, tid, cfg.weight_std, 0)
+            else:
+                device_fill(t.data_ptr(), t.numel(), seed, tid, gain_std, 1)
+            out[(key, layer)] = t
+    if host is None:
+        torch.cuda.synchronize()
+    return out
