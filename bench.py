@@ -1,0 +1,427 @@
+"""Benchmark of the batch-invariant block-verify step on GB300.
+
+Workload (default): Qwen3-8B-shaped random-init model (36 layers, hidden 4096,
+32 q / 8 kv heads, head_dim 128, SwiGLU 12288, vocab 151936, bf16), prompts of
+1024 uniform random ids, K = 4 verify rows per step ([pending, 3 drafts]),
+drafts taken from the target's own greedy chain with each slot replaced by a
+random id with probability 0.6; sequences of 64 generated tokens, one after
+another.  All inputs are seeded and synthetic.
+
+One "step" is one sv_verify of K rows: embed, 36 layers, LM head, argmax,
+acceptance and truncation.  Reported:
+  value   verified tokens/s with the step's inputs already in HBM
+          (sv_verify_async over device-resident windows), CUDA events on
+          the caller's stream around exactly --steps steps;
+  e2e     the same steps through sv_verify with host token arrays and host
+          results (H2D + D2H inside the timed region), wall clock;
+  roofline  the dominant kernel (the gate|up linear, 52% of a layer's bytes)
+          timed on the library stream, against the measured HBM peak;
+  cpu_baseline  the CPU oracle on a bounded sample (see "sample").
+`--impl reference` times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+
+METRIC = ("verify-step µs & verified tok/s, Qwen3-8B-shape K=4, 1 GB300; "
+          "% HBM roofline")
+GEN_TOKENS = 64  # generated tokens per sequence before the next sequence starts
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="qwen3-8b-shape", choices=sorted(inputs.CONFIGS))
+    ap.add_argument("--K", type=int, default=4)
+    ap.add_argument("--prefix", type=int, default=1024)
+    ap.add_argument("--p", type=float, default=0.6, help="per-slot draft corruption probability")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-layers", type=int, default=4,
+                    help="layers of the model the CPU oracle sample runs")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.th.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+def build_sequences(ctx_factory, cfg, K, steps_needed, prefix_len, p):
+    """Contexts with their prompt prefilled and greedy chain precomputed,
+    enough sequences for `steps_needed` verify steps of GEN_TOKENS each."""
+    seqs, total = [], 0
+    s = 0
+    while total < steps_needed:
+        ctx = ctx_factory()
+        prompt = inputs.prefix_tokens(s, prefix_len, cfg.vocab)
+        t = ctx.prefill(prompt)
+        chain = [t]
+        for _ in range(GEN_TOKENS + K):
+            t = ctx.decode(t)
+            chain.append(t)
+        ctx.truncate(prefix_len)
+        # steps of this sequence until GEN_TOKENS tokens are generated
+        sched, i, st = [], 0, 0
+        while i < GEN_TOKENS and total + len(sched) < steps_needed:
+            toks, n_exp = inputs.window(chain, i, K, seq=s, step=st, p=p, vocab=cfg.vocab)
+            sched.append((i, toks, n_exp))
+            i += n_exp + 1
+            st += 1
+        seqs.append({"ctx": ctx, "prompt": prompt, "chain": chain, "sched": sched})
+        total += len(sched)
+        s += 1
+    return seqs
+
+
+def counters(accepted, proposed, tokens, verify_steps, seconds):
+    """Speculative-decoding counters, with the definitions of the bench line in
+    "Phase 23: Speculative Verify Parity" section 3: acceptance_rate =
+    accepted / proposed, tokens_per_target_step = tokens / target steps,
+    tok/s = tokens / time (= 1000 / TPOT in ms).  Here every target step is a
+    verify (the correction token is the argmax of the first rejected row, so
+    no separate commit or correction decode is run)."""
+    return {"acceptance_rate": accepted / max(proposed, 1),
+            "tokens_per_target_step": tokens / max(verify_steps, 1),
+            "tok_s": tokens / seconds if seconds > 0 else float("nan"),
+            "tpot_ms": 1000.0 * seconds / tokens if tokens else float("nan")}
+
+
+def aggregate(dev_ms, tokens, dist=None):
+    """Whole-job time and tokens over replicas: the slowest rank's time and the
+    sum of all ranks' tokens."""
+    if dist is None:
+        return dev_ms, tokens
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(dev_ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([int(tokens)], dtype=torch.int64, device=dev)
+    dist.all_reduce(n)
+    return float(t.item()), int(n.item())
+
+
+def step_bytes(cfg, K, pos):
+    """Algorithmic HBM bytes of one verify step at committed length pos:
+    every weight once, K/V read for pos+K positions and written for K,
+    K embedding rows, fp32 logits written."""
+    return (cfg.weight_bytes() + (pos + K) * cfg.kv_bytes_per_token()
+            + K * cfg.kv_bytes_per_token() + 2 * K * cfg.hidden + 4 * K * cfg.vocab)
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("k_linear.cu", "sv_ptx.cuh", "sv_internal.h"):
+        with open(os.path.join(ROOT, "greedy_speculative_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        if t.get("kernel_hash") == kernel_hash():
+            return t.get("traffic_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(cfg, K, windows, n_layers_sample, reps=1, warmup=0):
+    """Time the CPU oracle's verify step on cfg truncated to n_layers_sample
+    layers and to 0 layers; return seconds of a full-depth verify step,
+    estimated as t0 + (t_L - t0) * n_layers / n_layers_sample, per rep."""
+    import oracle
+    prompt = inputs.prefix_tokens(0, 8, cfg.vocab)
+    times = {}
+    for L in (0, n_layers_sample):
+        c = inputs.shrink(cfg, n_layers=L)
+        hw = inputs.host_weights(c, seed=0)
+        m = oracle.OracleModel(hw, 8 + K * (reps + warmup + 1) + 8)
+        m.prefill(prompt)
+        ts = []
+        for r in range(warmup + reps):
+            toks = windows[r % len(windows)]
+            base = len(m)
+            t0 = time.perf_counter()
+            m.verify(toks)
+            ts.append(time.perf_counter() - t0)
+            m.truncate(base)
+        times[L] = ts[warmup:]
+        del m, hw
+    per = [times[0][i] + (times[n_layers_sample][i] - times[0][i]) * cfg.n_layers / n_layers_sample
+           for i in range(reps)]
+    return per, oracle.threads()
+
+
+def run_reference(args):
+    cfg = inputs.CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    K = args.K
+    # windows from a greedy chain are not needed for timing: the oracle's cost
+    # does not depend on token values; use the prompt-seeded ids
+    windows = [inputs.prefix_tokens(100 + i, K, cfg.vocab) for i in range(8)]
+    per, cores = oracle_sample(cfg, K, windows, args.oracle_layers, reps=args.steps,
+                               warmup=args.warmup)
+    q = 1.0 - args.p  # per-slot match probability: E[n + 1] = 1 + q + ... + q^(K-1)
+    tok_per_step = sum(q ** j for j in range(K))
+    total_s = sum(per)
+    value = tok_per_step * len(per) / total_s
+    sample = (f"CPU oracle verify step of K={K} rows on the {cfg.name} model truncated to "
+              f"{args.oracle_layers} of {cfg.n_layers} layers and to 0 layers (LM head), prefix 8 ids; "
+              f"full-depth step time = t0 + (tL - t0) * {cfg.n_layers}/{args.oracle_layers}; "
+              f"tokens per step = expected n+1 at per-slot match {1 - args.p:.2f}; attention over the "
+              f"{args.prefix}-position context not included")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * total_s / len(per), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 rounding emulated)",
+            "data": "synthetic",
+            "config": {"workload": f"{cfg.name} K={K} verify, prefix {args.prefix}",
+                       "K": K, "prefix": args.prefix},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+
+    import greedy_speculative_decode_gb300 as sv
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    cfg = inputs.CONFIGS[args.config]
+    K, W, S = args.K, args.warmup, args.steps
+    hbm_peak, peak_kind = peaks()
+    stream = torch.cuda.current_stream()
+
+    weights = inputs.device_weights(cfg, seed=0, gain_std=0.0)
+    max_seq = args.prefix + GEN_TOKENS + 2 * K + 16
+    make_ctx = lambda: sv.Context(cfg, weights, max_k=max(K, 32), max_seq=max_seq, stream=stream)
+    seqs = build_sequences(make_ctx, cfg, K, W + S, args.prefix, args.p)
+    steps = [(sq, i, toks, n_exp) for sq in seqs for (i, toks, n_exp) in sq["sched"]]
+    assert len(steps) >= W + S
+
+    # ---------------- device-resident run (value)
+    win = torch.tensor([s[2] for s in steps], dtype=torch.int32, device="cuda")
+    res = torch.zeros((len(steps), 4), dtype=torch.int32, device="cuda")
+    logits = torch.empty((K, cfg.vocab), dtype=torch.float32, device="cuda")
+    for sq in seqs:
+        sq["ctx"].reserve(max_seq)
+    for j in range(W):
+        steps[j][0]["ctx"].verify_async(win[j], K, res[j], logits)
+    for sq in seqs:
+        sq["ctx"].sync()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.15)  # let the sampler start before the timed region
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(S + 1)]
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
+    evs[0].record(stream)
+    for j in range(W, W + S):
+        steps[j][0]["ctx"].verify_async(win[j], K, res[j], logits)
+        evs[j - W + 1].record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    for sq in seqs:
+        sq["ctx"].sync()
+    dev_ms = evs[0].elapsed_time(evs[S])
+    step_ms = [evs[j].elapsed_time(evs[j + 1]) for j in range(S)]
+    r = res.cpu().tolist()
+    mismatches, tokens, accepted, proposed, pos_sum = 0, 0, 0, 0, 0
+    for j in range(W + S):
+        sq, i, toks, n_exp = steps[j]
+        n, corr, new_len, status = r[j]
+        ok = (n == n_exp and corr == sq["chain"][i + n + 1] and status == 0 and
+              new_len == args.prefix + i + n + 1)
+        mismatches += 0 if ok else 1
+        if j >= W:
+            tokens += n + 1
+            accepted += n
+            proposed += K - 1
+            pos_sum += args.prefix + i
+    dev_ms, tokens_all = aggregate(dev_ms, tokens, dist)
+    value = tokens_all / (dev_ms / 1000.0)
+
+    # ---------------- end to end through sv_verify (host arrays, host results)
+    for sq in seqs:
+        sq["ctx"].truncate(args.prefix)
+    for j in range(W):
+        steps[j][0]["ctx"].verify(steps[j][2], logits)
+    torch.cuda.synchronize()
+    e2e_res = []
+    t0 = time.perf_counter()
+    for j in range(W, W + S):
+        e2e_res.append(steps[j][0]["ctx"].verify(steps[j][2], logits))
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    clk = clocks.stop()
+    for (n, corr), j in zip(e2e_res, range(W, W + S)):
+        if n != r[j][0] or corr != r[j][1]:
+            mismatches += 1
+    e2e_value = tokens / e2e_s
+
+    # ---------------- dominant kernel: the gate|up linear, timed on the library stream
+    ctx0 = seqs[0]["ctx"]
+    gu_us, gu_bytes = ctx0.time_linear(sv.SV_LIN_GATE_UP, K, reps=3)
+    achieved = gu_bytes / (gu_us * 1e-6) / 1e9
+    lin = {w: ctx0.time_linear(code, K, reps=3) for w, code in
+           (("o", sv.SV_LIN_O), ("down", sv.SV_LIN_DOWN), ("lm_head", sv.SV_LIN_LM_HEAD))}
+
+    mean_pos = pos_sum / S
+    sb = step_bytes(cfg, K, mean_pos)
+    ms_per_step = dev_ms / S
+    out = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": S,
+        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name} K={K} block verify, prefix {args.prefix} random ids, "
+                               f"{GEN_TOKENS} generated tokens per sequence, draft slots corrupted "
+                               f"with p={args.p}",
+                   "K": K, "prefix": args.prefix, "sequences": len(seqs),
+                   "l2": f"inputs larger than L2: {cfg.weight_bytes() / 1e9:.2f} GB of weights "
+                         f"streamed per step", "parallelism": "replicas"},
+        "verify_step_us": {"median": 1000 * statistics.median(step_ms),
+                           "p90": 1000 * sorted(step_ms)[int(0.9 * (len(step_ms) - 1))],
+                           "mean": 1000 * ms_per_step},
+        "step_bytes": sb,
+        "hbm_frac_step": sb / (ms_per_step / 1000.0) / 1e9 / hbm_peak,
+        **{k: v for k, v in counters(accepted, proposed, tokens, S, dev_ms / 1000.0).items()
+           if k in ("acceptance_rate", "tokens_per_target_step")},
+        "verify_decode_mismatches": mismatches,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": ncu_traffic(),
+                     "kernel": "k_linear (gate|up + SwiGLU epilogue)", "peak_kind": peak_kind,
+                     "launch_us": gu_us, "bytes_per_launch": gu_bytes},
+        "linears_us": {w: {"us": u, "GB/s": b / (u * 1e-6) / 1e9} for w, (u, b) in lin.items()},
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": 4 * (K + 1),
+                "d2h_bytes_per_step": 16},
+        "gpu_launches": ctx0.kernels_per_step(K) * S,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        windows = [s[2] for s in steps[:4]]
+        per, cores = oracle_sample(cfg, K, windows, args.oracle_layers, reps=2)
+        out["cpu_baseline"] = {
+            "value": (tokens / S) / statistics.median(per), "unit": "tok/s", "cores": cores,
+            "kind": "oracle",
+            "sample": (f"2 verify steps of K={K} on the {cfg.name} model truncated to "
+                       f"{args.oracle_layers} of {cfg.n_layers} layers and to 0 layers, prefix 8 "
+                       f"ids; full step = t0 + (tL - t0) * {cfg.n_layers}/{args.oracle_layers}; "
+                       f"tokens per step as measured on the GPU; the {args.prefix}-position "
+                       f"attention not included")}
+    if rank == 0:
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

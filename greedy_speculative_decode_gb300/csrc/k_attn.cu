@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1)
         mma_bf16(o[2 * dn], afr, b0, b1);
         mma_bf16(o[2 * dn + 1], afr, b2, b3);
       }
+      fence_proxy_async_smem();  // reads of buffer b precede its next TMA write
       __syncwarp();
       if (lane == 0 && j + C::kBufs < npages) issue(j + C::kBufs);
     }
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1)
       *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
       *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
-    __syncthreads();  // scratch (= ring) and Qs are rewritten by the next item
+    fence_proxy_async_smem();  // scratch (in the ring) is overwritten by TMA next item
+    __syncthreads();            // scratch (= ring) and Qs are rewritten by the next item
   }
 }
 

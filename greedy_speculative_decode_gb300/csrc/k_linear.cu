@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kLinThreads, 2)
         mma_bf16(acc[t], a, b0, b1);
       }
     }
+    fence_proxy_async_smem();  // our ldmatrix reads of stage s precede its next TMA write
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
   }

@@ -27,6 +27,7 @@ struct sv_ctx {
   cudaStream_t user_stream = nullptr, stream = nullptr;
   cudaEvent_t ev = nullptr;
   bool use_graphs = true;
+  bool use_pdl = true;  // chain a step's kernels with programmatic dependent launch
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
   std::vector<const bf16*> attn_norm, q_norm, k_norm, ffn_norm;
@@ -213,11 +214,11 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       p.vcache = ctx->vpool + loff;
       p.q_gain = c.qk_norm ? ctx->q_norm[l] : nullptr;
       p.k_gain = c.qk_norm ? ctx->k_norm[l] : nullptr;
-      CK(launch_linear(ld, p, EPI_QKV, true, s, true));
+      CK(launch_linear(ld, p, EPI_QKV, true, s, ctx->use_pdl));
     }
     ap.layer = l;
-    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, s, true));
-    CK(launch_attn_combine(ap, d, s, true));
+    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, s, ctx->use_pdl));
+    CK(launch_attn_combine(ap, d, s, ctx->use_pdl));
     {  // attention projection + residual
       LinParams p = base;
       const LinearDesc& ld = ctx->lin_o[l];
@@ -226,7 +227,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       p.out = ctx->x;
       p.out_stride = H;
       p.out_ss = ctx->x_ss;
-      CK(launch_linear(ld, p, EPI_RESID, false, s, true));
+      CK(launch_linear(ld, p, EPI_RESID, false, s, ctx->use_pdl));
     }
     {  // RMSNorm + gate|up + activation
       LinParams p = base;
@@ -237,7 +238,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
       p.out = ctx->a;
       p.out_stride = c.ffn;
-      CK(launch_linear(ld, p, EPI_GLU, true, s, true));
+      CK(launch_linear(ld, p, EPI_GLU, true, s, ctx->use_pdl));
     }
     {  // down projection + residual
       LinParams p = base;
@@ -247,7 +248,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       p.out = ctx->x;
       p.out_stride = H;
       p.out_ss = ctx->x_ss;
-      CK(launch_linear(ld, p, EPI_RESID, false, s, true));
+      CK(launch_linear(ld, p, EPI_RESID, false, s, ctx->use_pdl));
     }
   }
   if (mode != MODE_BODY) {  // final RMSNorm + LM head + per-tile argmax
@@ -261,10 +262,10 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
     p.logits_row0 = (mode == MODE_PREFILL) ? M - 1 : 0;
     p.am_val = ctx->am_val;
     p.am_idx = ctx->am_idx;
-    CK(launch_linear(ld, p, EPI_LOGITS, true, s, true));
+    CK(launch_linear(ld, p, EPI_LOGITS, true, s, ctx->use_pdl));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
-                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s, true));
+                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s, ctx->use_pdl));
   return SV_OK;
 }
 
@@ -418,6 +419,8 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   if (cudaEventCreateWithFlags(&ctx->ev, cudaEventDisableTiming) != cudaSuccess) return bail(SV_E_CUDA);
   const char* ng = getenv("SV_NO_GRAPHS");
   ctx->use_graphs = !(ng && ng[0] == '1');
+  const char* np = getenv("SV_NO_PDL");
+  ctx->use_pdl = !(np && np[0] == '1');
   if (prepare_linear_kernels() != cudaSuccess || prepare_attention_kernels() != cudaSuccess)
     return bail(SV_E_CUDA);
 
@@ -572,10 +575,8 @@ int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits
   if (!ctx) return SV_E_INVAL;
   if (K < 1 || K > ctx->cfg.max_k) return fail(ctx, SV_E_INVAL, "K=%d outside [1, %d]", K, ctx->cfg.max_k);
   if (!tokens_dev || !result_dev) return fail(ctx, SV_E_INVAL, "null device pointer");
-  if (!ctx->async_pending) {
-    CK(cudaEventRecord(ctx->ev, ctx->user_stream));
-    CK(cudaStreamWaitEvent(ctx->stream, ctx->ev, 0));
-  }
+  CK(cudaEventRecord(ctx->ev, ctx->user_stream));
+  CK(cudaStreamWaitEvent(ctx->stream, ctx->ev, 0));
   ctx->async_pending = true;
   CK(cudaMemcpyAsync(ctx->st->tokens, tokens_dev, K * sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
   int rc = run_step(ctx, K, MODE_VERIFY, logits_dev);

@@ -32,6 +32,15 @@ __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order this thread's earlier generic-proxy accesses of shared memory (plain
+// loads/stores, ldmatrix) before later async-proxy (TMA) accesses of the same
+// bytes.  A buffer that threads have read must pass through this fence before
+// it is handed back to be overwritten by TMA: without it the TMA write may
+// land before the reads, which showed up as rare wrong tiles.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
