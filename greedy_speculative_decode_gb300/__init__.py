@@ -65,11 +65,13 @@ def _load():
     L.sv_step_kernel_count.argtypes = [_P, _i32, _i32]
     L.sv_time_linear.argtypes = [_P, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_float),
                                  ctypes.POINTER(ctypes.c_double)]
+    L.sv_lm_head_noalloc.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_float, _P, _P, _P, _P]
     L.sv_last_error.argtypes = [_P]
     L.sv_last_error.restype = ctypes.c_char_p
     for name in ("sv_create", "sv_prefill", "sv_decode", "sv_verify", "sv_verify_async",
                  "sv_reserve", "sv_sync", "sv_truncate", "sv_seq_len", "sv_kv_read",
-                 "sv_shuffle_pages", "sv_step_kernel_count", "sv_time_linear"):
+                 "sv_shuffle_pages", "sv_step_kernel_count", "sv_time_linear",
+                 "sv_lm_head_noalloc"):
         getattr(L, name).restype = _i32
     return L
 
@@ -88,6 +90,22 @@ def _i32_array(vals):
 
 def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
+
+
+def lm_head_noalloc(x, gain, w, logits, argmax=None, status=None, eps=1e-6, stream=None):
+    """sv_lm_head_noalloc: logits and greedy tokens of M rows without any
+    device allocation by the library (scratch is a fixed array inside it).
+    x: bf16 [M, hidden]; gain: bf16 [hidden]; w: bf16 [vocab, hidden];
+    logits: fp32 [M, vocab]; argmax: int32 [M] or None; status: int32 [1] or
+    None. All CUDA tensors owned by the caller. Asynchronous on `stream`."""
+    M, hidden = int(x.shape[0]), int(x.shape[1])
+    vocab = int(w.shape[0])
+    s = _P(stream.cuda_stream) if stream is not None else _P(0)
+    rc = _lib.sv_lm_head_noalloc(_P(_ptr(x)), _P(_ptr(gain)), _P(_ptr(w)), M, hidden, vocab,
+                                 float(eps), _P(_ptr(logits)), _P(_ptr(argmax)), _P(_ptr(status)), s)
+    if rc != SV_OK:
+        raise SvError(rc, "sv_lm_head_noalloc rejected the shapes (scratch limit 8 MiB, "
+                          "1 <= M <= 32, hidden % 128 == 0) or a CUDA call failed")
 
 
 class Context:

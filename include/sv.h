@@ -166,6 +166,37 @@ int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head);
 #define SV_LIN_LM_HEAD 4
 int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, double* bytes_per_launch);
 
+/* LM-head step that allocates no device memory.  There is no counterpart to
+ * this call on the pages the library follows; it exists for callers that may
+ * not call cudaMalloc: code running in a process whose GPU memory is already
+ * reserved by another allocator (a serving runtime's pool, or a plugin inside
+ * one), and latency-critical code that cannot accept the device-wide
+ * synchronisation an allocation may cause.
+ *
+ * Computes, for M rows x (bf16 [M, hidden], device):
+ *   logits = bf16(RMSNorm(x; gain, eps) . W^T)   as fp32 [M, vocab] (device)
+ *   argmax[m] = greedy token of row m (largest logit, lowest id on ties)
+ * with the same batch-invariant linear kernel, K split and rounding as the
+ * context's LM head; for a model with no layers its logits equal sv_verify's.
+ *   gain: bf16 [hidden]; W: bf16 [vocab, hidden]; all inputs 16-byte aligned.
+ *   argmax_dev: int32 [M] or NULL; status_dev: int32 [1] or NULL, set to 0, or
+ *     to the kernels' failure bits (1 timeout).
+ *   cuda_stream: the stream to run on (NULL = legacy stream).  Asynchronous.
+ * Scratch: the split-K partial tiles, their tickets, the argmax partials and
+ * the row statistics live in one fixed 8 MiB device array inside the library
+ * (held on every GPU that loads it until the process exits).  Shapes whose
+ * scratch would not fit return SV_E_NOMEM; the rough bound is
+ *   4 * ceil(vocab/128) * splits * 128 * (8, 16 or 32 for M <= 8, 16, 32)
+ *   bytes <= 8 MiB, with splits = hidden/1024 for hidden >= 1024.
+ * Other limits: 1 <= M <= 32, hidden % 128 == 0 (else SV_E_INVAL).
+ * The first call on a device looks up the array's address and sets kernel
+ * attributes for that device; make that first call before any stream capture.
+ * Every call uses the same array: calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller. */
+int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const void* w_dev, int M, int hidden,
+                       int vocab, float eps, float* logits_dev, int32_t* argmax_dev,
+                       int32_t* status_dev, void* cuda_stream);
+
 const char* sv_last_error(const sv_ctx* ctx);
 
 #ifdef __cplusplus

@@ -1,0 +1,65 @@
+"""The allocation-free LM-head call (sv_lm_head_noalloc) against the context
+path that owns its buffers.
+
+Callers of the allocation-free call are those that may not cudaMalloc: code
+inside a process whose device memory another allocator has already reserved
+(a serving runtime's pool or a plugin in it), and latency-critical code that
+cannot take the synchronisation an allocation may bring. For a model with no
+layers, sv_verify computes exactly embed -> final RMSNorm -> LM head ->
+argmax, so its logits are the reference for this call on the same rows.
+This file is collected last so a failure here leaves every other test run.
+"""
+import pytest
+
+import inputs
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _compare(cfg, tokens, seed):
+    import greedy_speculative_decode_gb300 as sv
+    dw = inputs.device_weights(cfg, seed=seed, gain_std=0.1)
+    K = len(tokens)
+    ctx = gh.context(cfg, dw, max_k=32, max_seq=64)
+    ref = gh.logits_buf(K, cfg.vocab)
+    ctx.verify(tokens, logits=ref)
+    ref_am = ref.argmax(dim=1).to(torch.int32)
+    ctx.close()
+    x = dw[("embed", -1)][torch.tensor(tokens, device="cuda")].contiguous()
+    gain = dw[("final_norm", -1)]
+    w = dw.get(("lm_head", -1), dw[("embed", -1)])
+    for call in range(2):  # two calls in a row share the fixed scratch array
+        lg = gh.logits_buf(K, cfg.vocab)
+        am = torch.full((K,), -1, dtype=torch.int32, device="cuda")
+        st = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+        sv.lm_head_noalloc(x, gain, w, lg, am, st, eps=cfg.rms_eps)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, f"call {call}: kernel status {int(st.item())}"
+        err = (lg.double() - ref.double()).abs().max().item()
+        assert err <= gh.TOL_LOGIT, f"call {call}: max |dlogit| {err}"
+        top2 = torch.topk(ref, 2, dim=1).values
+        sure = (top2[:, 0] - top2[:, 1]) > gh.ARGMAX_MARGIN
+        assert torch.equal(am[sure], ref_am[sure]), f"call {call}: argmax differs"
+
+
+def test_no_alloc_lm_head_matches_context_tiny():
+    cfg = inputs.shrink(inputs.TINY, n_layers=0)
+    _compare(cfg, [5, 77, 901, 3, 1023], seed=3)
+
+
+def test_no_alloc_lm_head_matches_context_wide():
+    cfg = inputs.shrink(inputs.QWEN3_8B, n_layers=0, vocab=32768)
+    _compare(cfg, [11, 2049, 30000, 7], seed=4)
+
+
+def test_no_alloc_rejects_shapes_beyond_the_scratch():
+    import greedy_speculative_decode_gb300 as sv
+    x = torch.zeros((4, 4096), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones((4096,), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((151936, 4096), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((4, 151936), dtype=torch.float32, device="cuda")
+    with pytest.raises(sv.SvError) as e:
+        sv.lm_head_noalloc(x, g, w, lg)
+    assert e.value.code == sv.SV_E_NOMEM
