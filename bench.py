@@ -55,6 +55,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-layers", type=int, default=4,
                     help="layers of the model the CPU oracle sample runs")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="use only the first N layers of the model (profiling cases)")
+    ap.add_argument("--vocab", type=int, default=None, help="override the vocabulary size")
+    ap.add_argument("--linear-only", action="store_true",
+                    help="time each linear class once per layer (NVTX range 'linear') and exit")
     return ap.parse_args()
 
 
@@ -271,10 +276,42 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+def model_config(args):
+    cfg = inputs.CONFIGS[args.config]
+    kw = {}
+    if args.layers is not None:
+        kw["n_layers"] = args.layers
+    if args.vocab is not None:
+        kw["vocab"] = args.vocab
+    return inputs.shrink(cfg, **kw) if kw else cfg
+
+
+def run_linear_only(args):
+    """Small profiling case: each linear class of the model timed on its own."""
+    import torch
+
+    import greedy_speculative_decode_gb300 as sv
+    cfg = model_config(args)
+    weights = inputs.device_weights(cfg, seed=0, gain_std=0.0)
+    ctx = sv.Context(cfg, weights, max_k=max(args.K, 32), max_seq=64)
+    ctx.prefill(inputs.prefix_tokens(0, 8, cfg.vocab))
+    out = {}
+    torch.cuda.nvtx.range_push("linear")
+    for name, code in (("o", sv.SV_LIN_O), ("gate_up", sv.SV_LIN_GATE_UP),
+                       ("down", sv.SV_LIN_DOWN), ("lm_head", sv.SV_LIN_LM_HEAD)):
+        us, b = ctx.time_linear(code, args.K, reps=1)
+        out[name] = {"us": us, "GB/s": b / (us * 1e-6) / 1e9, "bytes": b}
+    torch.cuda.nvtx.range_pop()
+    print(json.dumps({"config": cfg.name, "layers": cfg.n_layers, "vocab": cfg.vocab, "K": args.K,
+                      "linears": out}))
+
+
 def run_ours(args):
     import torch
 
     import greedy_speculative_decode_gb300 as sv
+    if args.linear_only:
+        return run_linear_only(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -285,7 +322,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
 
-    cfg = inputs.CONFIGS[args.config]
+    cfg = model_config(args)
     K, W, S = args.K, args.warmup, args.steps
     hbm_peak, peak_kind = peaks()
     stream = torch.cuda.current_stream()

@@ -213,28 +213,78 @@ __device__ void epilogue_logits(const LinParams& p, int tile, float* T, int TS) 
   }
 }
 
+// Owner of flattened k-block kb under the even split of T k-blocks over G CTAs
+// (CTA c owns [c T / G, (c + 1) T / G)).
+__device__ __forceinline__ int owner_cta(long long kb, long long T, int G) {
+  return (int)(((kb + 1) * G - 1) / T);
+}
+
+// Stage input columns c0 + t (mod Kd), t in [t0, t0 + ncols), of the M rows
+// into xs (row stride XS), RMS-normalising them when NORM; rows M..MP-1 and
+// columns past ncols are zero.  c0, t0 and Kd are multiples of 64.
+template <int MP, int XS, bool NORM>
+__device__ __forceinline__ void stage_x(const LinParams& p, bf16* xs, int c0, int t0, int ncols,
+                                        const float* s_rstd, int tid, int nthr) {
+  constexpr int VPR = (XS - 8) / 8;  // 16-byte vectors per staged row
+  for (int v = tid; v < MP * VPR; v += nthr) {
+    const int m = v / VPR, c8 = v % VPR;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (m < p.M && c8 * 8 < ncols) {
+      int k = c0 + t0 + c8 * 8;
+      if (k >= p.Kd) k -= p.Kd;
+      val = *reinterpret_cast<const uint4*>(p.X + (size_t)m * p.Kd + k);
+      if (NORM) {
+        const float r = s_rstd[m];
+        const uint4 gv = *reinterpret_cast<const uint4*>(p.gain + k);
+        const bf16* xb = reinterpret_cast<const bf16*>(&val);
+        const bf16* gb = reinterpret_cast<const bf16*>(&gv);
+        uint32_t w[4];
+        for (int j = 0; j < 4; ++j) {
+          float y0 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * j]), r)),
+                                     __bfloat162float(gb[2 * j])));
+          float y1 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * j + 1]), r)),
+                                     __bfloat162float(gb[2 * j + 1])));
+          w[j] = pack_bf16x2(y0, y1);
+        }
+        val = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    *reinterpret_cast<uint4*>(xs + (size_t)m * XS + c8 * 8) = val;
+  }
+}
+
+// Persistent stream-K linear.  The n_tiles x (Kd/64) k-blocks of the weight,
+// tile-major, are cut into gridDim.x equal contiguous ranges, one per CTA.
+// A tile whose k-blocks all fall in one CTA is finished there; a tile cut by
+// range boundaries is finished by the last of its CTAs to arrive, which sums
+// the per-CTA partials in k order.  The partition depends only on the weight
+// shape and the grid (one CTA per SM), never on M.
 template <int MT, int EPI, bool NORM>
-__global__ void __launch_bounds__(kLinThreads, 2)
+__global__ void __launch_bounds__(kLinThreads, 1)
     k_linear(const __grid_constant__ CUtensorMap wmap, const LinParams p) {
-  constexpr int MP = MT * 8;  // padded token rows
-  constexpr int TS = MP + 1;  // epilogue tile row stride (floats)
+  constexpr int MP = MT * 8;                                  // padded token rows
+  constexpr int TS = MP + 1;                                  // epilogue tile row stride
+  constexpr int XC = kLinXCols / MT;  // input columns staged at once
+  constexpr int XS = XC + 8;          // staged row stride in elements (16B pad: no bank conflicts)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* ring = smem;
-  const int xs_stride = p.Kc + 8;  // bf16 elements per staged row (16B pad vs bank conflicts)
   bf16* xs = reinterpret_cast<bf16*>(smem + kLinStages * kLinStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xs) +
-                                               (size_t)MP * xs_stride * sizeof(bf16));
+  float* T = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + MP * XS * sizeof(bf16));
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(T) +
+                                               ((kLinRows * TS * sizeof(float) + 15) & ~size_t(15)));
   uint64_t* empty = full + kLinStages;
-  float* s_rstd = reinterpret_cast<float*>(empty + kLinStages);  // [64]
-  int* s_flag = reinterpret_cast<int*>(s_rstd + 64);
+  float* s_rstd = reinterpret_cast<float*>(empty + kLinStages);  // [32] row rstd of the input
+  float* s_hrstd = s_rstd + kMaxK;                               // [64] per-head rstd (QKV)
+  int* s_flag = reinterpret_cast<int*>(s_hrstd + 64);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-  const int k0 = split * p.Kc;
-  const int n_iter = p.Kc / kLinBK;
-  const TileRows tr = tile_rows(p, tile);
+  const int KB = p.Kd / kLinBK;
+  const long long Tk = (long long)p.n_tiles * KB;
+  const int G = gridDim.x;
+  const long long kb_begin = (long long)blockIdx.x * Tk / G;
+  const long long kb_end = (long long)(blockIdx.x + 1) * Tk / G;
 
   if (tid == 0) {
     for (int s = 0; s < kLinStages; ++s) {
@@ -253,15 +303,21 @@ __global__ void __launch_bounds__(kLinThreads, 2)
       prefetch_tensormap(&wmap);
       const uint64_t pol = policy_evict_first();
       bool ok = true;
-      for (int it = 0; it < n_iter && ok; ++it) {
+      int it = 0;
+      int tile = (int)(kb_begin / KB), kk = (int)(kb_begin % KB);  // walked without division
+      for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
         const int s = it % kLinStages;
         if (it >= kLinStages) ok = mbar_wait(&empty[s], ((it / kLinStages) & 1) ^ 1);
         if (!ok) break;
+        const TileRows tr = tile_rows(p, tile);
         mbar_arrive_expect_tx(&full[s], kLinStageBytes);
         uint8_t* dst = ring + s * kLinStageBytes;
-        const int kc = k0 + it * kLinBK;
-        tma_load_2d(dst, &wmap, kc, tr.a0, &full[s], pol);
-        tma_load_2d(dst + kLinChunkBytes, &wmap, kc, tr.b0, &full[s], pol);
+        tma_load_2d(dst, &wmap, kk * kLinBK, tr.a0, &full[s], pol);
+        tma_load_2d(dst + kLinChunkBytes, &wmap, kk * kLinBK, tr.b0, &full[s], pol);
+        if (++kk == KB) {
+          kk = 0;
+          ++tile;
+        }
       }
       if (!ok) atomicOr(&p.st->status, ST_TIMEOUT);
     }
@@ -277,134 +333,136 @@ __global__ void __launch_bounds__(kLinThreads, 2)
       for (int t = 0; t < p.ss_tiles; ++t) ss = __fadd_rn(ss, p.x_ss[tid * p.ss_tiles + t]);
       s_rstd[tid] = 1.0f / sqrtf(ss / (float)p.Kd + p.eps);
     }
-    named_sync(1, nthr);
   }
-  {
-    const int vec_per_row = p.Kc / 8;
-    for (int v = tid; v < MP * vec_per_row; v += nthr) {
-      const int m = v / vec_per_row, c8 = v % vec_per_row;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (m < p.M) {
-        const int k = k0 + c8 * 8;
-        val = *reinterpret_cast<const uint4*>(p.X + (size_t)m * p.Kd + k);
-        if (NORM) {
-          const float r = s_rstd[m];
-          const uint4 gv = *reinterpret_cast<const uint4*>(p.gain + k);
-          const bf16* xb = reinterpret_cast<const bf16*>(&val);
-          const bf16* gb = reinterpret_cast<const bf16*>(&gv);
-          uint32_t w[4];
-          for (int j = 0; j < 4; ++j) {
-            float y0 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * j]), r)),
-                                       __bfloat162float(gb[2 * j])));
-            float y1 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * j + 1]), r)),
-                                       __bfloat162float(gb[2 * j + 1])));
-            w[j] = pack_bf16x2(y0, y1);
-          }
-          val = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      *reinterpret_cast<uint4*>(xs + (size_t)m * xs_stride + c8 * 8) = val;
-    }
-  }
-  named_sync(1, nthr);
 
   const int chunk = warp >> 2, rg = warp & 3;
+  const int g = lane >> 2, q = lane & 3;
+  const int lr0 = chunk * 64 + rg * 16 + g;
+  const int a_row = rg * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);  // row within the 64-row chunk
+  const int a_khalf = lane >> 4;
+  const uint32_t xs_base =
+      smem_u32(xs) + (uint32_t)(((lane & 7) * XS + ((lane >> 3) & 1) * 8) * sizeof(bf16));
   float acc[MT][4];
 #pragma unroll
   for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
 
-  // per-lane ldmatrix geometry
-  const int a_row = rg * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);  // row within the 64-row chunk
-  const int a_khalf = lane >> 4;
-  const uint32_t xs_base = smem_u32(xs) +
-                           (uint32_t)(((lane & 7) * xs_stride + ((lane >> 3) & 1) * 8) * sizeof(bf16));
+  // The input columns this CTA reads form one circular window of Kd starting
+  // at its first k-block; it is staged XC columns at a time, usually once.
+  const int c0 = (int)(kb_begin % KB) * kLinBK;
+  const int ncols = (int)((kb_end - kb_begin) * kLinBK < p.Kd ? (kb_end - kb_begin) * kLinBK : p.Kd);
   bool ok = true;
-  for (int it = 0; it < n_iter; ++it) {
-    const int s = it % kLinStages;
-    if (!mbar_wait(&full[s], (it / kLinStages) & 1)) {
-      ok = false;
-      break;
+  int staged = -1;
+  long long seg_begin = kb_begin;
+  int it = 0;
+  int tile_c = (int)(kb_begin / KB), kk_c = (int)(kb_begin % KB);  // walked without division
+  for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
+    const int tile = tile_c, kk = kk_c;
+    if (++kk_c == KB) {
+      kk_c = 0;
+      ++tile_c;
     }
-    const uint32_t tile_base = smem_u32(ring + s * kLinStageBytes + chunk * kLinChunkBytes);
+    int jw = kk * kLinBK - c0;  // column offset within the window
+    if (jw < 0) jw += p.Kd;
+    const int xchunk = jw / XC;
+    if (xchunk != staged) {
+      named_sync(1, nthr);  // all warps are done with the previous chunk (and s_rstd is set)
+      stage_x<MP, XS, NORM>(p, xs, c0, xchunk * XC, min(XC, ncols - xchunk * XC), s_rstd, tid, nthr);
+      named_sync(1, nthr);
+      staged = xchunk;
+    }
+    const int s = it % kLinStages;
+    if (ok && !mbar_wait(&full[s], (it / kLinStages) & 1)) ok = false;
+    if (ok) {
+      const uint32_t tile_base = smem_u32(ring + s * kLinStageBytes + chunk * kLinChunkBytes);
+      const uint32_t xcol = (uint32_t)(jw - xchunk * XC);
 #pragma unroll
-    for (int kk = 0; kk < kLinBK / 16; ++kk) {
-      uint32_t a[4];
-      const int kchunk = kk * 2 + a_khalf;
-      ldsm_x4(tile_base + a_row * 128 + ((kchunk ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+      for (int k16 = 0; k16 < kLinBK / 16; ++k16) {
+        uint32_t a[4];
+        const int kc = k16 * 2 + a_khalf;
+        ldsm_x4(tile_base + a_row * 128 + ((kc ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        uint32_t b0, b1;
-        ldsm_x2(xs_base + (uint32_t)(((t * 8) * xs_stride + it * kLinBK + kk * 16) * sizeof(bf16)),
-                b0, b1);
-        mma_bf16(acc[t], a, b0, b1);
+        for (int t = 0; t < MT; ++t) {
+          uint32_t b0, b1;
+          ldsm_x2(xs_base + (uint32_t)(((t * 8) * XS + xcol + k16 * 16) * sizeof(bf16)), b0, b1);
+          mma_bf16(acc[t], a, b0, b1);
+        }
       }
     }
     fence_proxy_async_smem();  // our ldmatrix reads of stage s precede its next TMA write
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
+
+    if (kk != KB - 1 && kb != kb_end - 1) continue;
+    // ------------ this CTA's part of `tile` is complete
+    const int kk_first = kb - seg_begin >= kk ? 0 : kk - (int)(kb - seg_begin);
+    seg_begin = kb + 1;
+    named_sync(1, nthr);  // the previous tile's epilogue is done with T
+    if (kk_first == 0 && kk == KB - 1) {
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int m0 = t * 8 + 2 * q;
+        T[lr0 * TS + m0] = acc[t][0];
+        T[lr0 * TS + m0 + 1] = acc[t][1];
+        T[(lr0 + 8) * TS + m0] = acc[t][2];
+        T[(lr0 + 8) * TS + m0 + 1] = acc[t][3];
+      }
+    } else {
+      const int c_first = owner_cta((long long)tile * KB, Tk, G);
+      const int c_last = owner_cta((long long)tile * KB + KB - 1, Tk, G);
+      const int nseg = c_last - c_first + 1, seg = blockIdx.x - c_first;
+      float* wsb = p.ws + ((size_t)(tile * p.max_seg + seg) * kLinRows) * MP;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int m0 = t * 8 + 2 * q;
+        *reinterpret_cast<float2*>(wsb + lr0 * MP + m0) = make_float2(acc[t][0], acc[t][1]);
+        *reinterpret_cast<float2*>(wsb + (lr0 + 8) * MP + m0) = make_float2(acc[t][2], acc[t][3]);
+      }
+      __threadfence();
+      named_sync(1, nthr);
+      if (tid == 0) {
+        const int prev = atomicAdd(&p.counters[tile], 1);
+        *s_flag = (prev == nseg - 1);
+      }
+      named_sync(1, nthr);
+      const bool last = *s_flag != 0;
+      if (last) {
+        __threadfence();
+        // last CTA of this tile: sum the partials of its CTAs in k order
+        const float* wst = p.ws + ((size_t)tile * p.max_seg * kLinRows) * MP;
+        for (int e = tid; e < kLinRows * p.M; e += nthr) {
+          const int lr = e / p.M, m = e % p.M;
+          float v = __ldcg(wst + lr * MP + m);
+          for (int j = 1; j < nseg; ++j)
+            v = __fadd_rn(v, __ldcg(wst + ((size_t)j * kLinRows + lr) * MP + m));
+          T[lr * TS + m] = v;
+        }
+        if (tid == 0) p.counters[tile] = 0;  // ready for the next launch
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+      if (!last) continue;
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    named_sync(1, nthr);
+    if (EPI == EPI_QKV)
+      epilogue_qkv(p, tile, T, TS, s_hrstd);
+    else if (EPI == EPI_RESID)
+      epilogue_resid(p, tile, T, TS);
+    else if (EPI == EPI_GLU)
+      epilogue_glu(p, tile, T, TS);
+    else
+      epilogue_logits(p, tile, T, TS);
   }
   if (!ok && lane == 0) atomicOr(&p.st->status, ST_TIMEOUT);
-
-  // All stages consumed (or abandoned): reuse the ring for the fp32 tile.
-  named_sync(1, nthr);
-  float* T = reinterpret_cast<float*>(ring);
-  const int g = lane >> 2, q = lane & 3;
-  const int lr0 = chunk * 64 + rg * 16 + g;
-  if (p.splits == 1) {
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      const int m0 = t * 8 + 2 * q;
-      T[lr0 * TS + m0] = acc[t][0];
-      T[lr0 * TS + m0 + 1] = acc[t][1];
-      T[(lr0 + 8) * TS + m0] = acc[t][2];
-      T[(lr0 + 8) * TS + m0 + 1] = acc[t][3];
-    }
-  } else {
-    float* wsb = p.ws + ((size_t)(tile * p.splits + split) * kLinRows) * MP;
-#pragma unroll
-    for (int t = 0; t < MT; ++t) {
-      const int m0 = t * 8 + 2 * q;
-      *reinterpret_cast<float2*>(wsb + lr0 * MP + m0) = make_float2(acc[t][0], acc[t][1]);
-      *reinterpret_cast<float2*>(wsb + (lr0 + 8) * MP + m0) = make_float2(acc[t][2], acc[t][3]);
-    }
-    __threadfence();
-    named_sync(1, nthr);
-    if (tid == 0) {
-      int prev = atomicAdd(&p.counters[tile], 1);
-      *s_flag = (prev == p.splits - 1);
-    }
-    named_sync(1, nthr);
-    if (!*s_flag) return;
-    __threadfence();
-    // Last CTA of this tile: sum the split partials in split order.
-    const float* wst = p.ws + ((size_t)tile * p.splits * kLinRows) * MP;
-    for (int e = tid; e < kLinRows * p.M; e += nthr) {
-      const int lr = e / p.M, m = e % p.M;
-      float v = __ldcg(wst + lr * MP + m);
-      for (int sp = 1; sp < p.splits; ++sp)
-        v = __fadd_rn(v, __ldcg(wst + ((size_t)sp * kLinRows + lr) * MP + m));
-      T[lr * TS + m] = v;
-    }
-    if (tid == 0) p.counters[tile] = 0;  // ready for the next launch
-  }
-  named_sync(1, nthr);
-
-  if (EPI == EPI_QKV)
-    epilogue_qkv(p, tile, T, TS, s_rstd);
-  else if (EPI == EPI_RESID)
-    epilogue_resid(p, tile, T, TS);
-  else if (EPI == EPI_GLU)
-    epilogue_glu(p, tile, T, TS);
-  else
-    epilogue_logits(p, tile, T, TS);
 }
 
 template <int MT, int EPI, bool NORM>
 cudaError_t launch_t(const LinearDesc& d, const LinParams& p, cudaStream_t s, bool pdl) {
-  const size_t smem = linear_smem_bytes(MT, d.Kc);
+  const size_t smem = linear_smem_bytes(MT);
   auto kern = k_linear<MT, EPI, NORM>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(d.n_tiles * d.splits);
+  cfg.gridDim = dim3(d.grid);
   cfg.blockDim = dim3(kLinThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -419,7 +477,7 @@ cudaError_t launch_t(const LinearDesc& d, const LinParams& p, cudaStream_t s, bo
 template <int MT, int EPI, bool NORM>
 cudaError_t prepare_t() {
   return cudaFuncSetAttribute(k_linear<MT, EPI, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)linear_smem_bytes(MT, kLinKcMax));
+                              (int)linear_smem_bytes(MT));
 }
 
 template <int MT>
@@ -449,14 +507,28 @@ cudaError_t launch_mt(const LinearDesc& d, const LinParams& p, int epi, bool nor
 
 }  // namespace
 
-size_t linear_smem_bytes(int mt, int Kc) {
+size_t linear_smem_bytes(int mt) {
+  const int mp = mt * 8;
+  const int xc = kLinXCols / mt;
   size_t b = 1024;  // alignment slack
   b += (size_t)kLinStages * kLinStageBytes;
-  b += (size_t)mt * 8 * (Kc + 8) * sizeof(bf16);
-  b += 2 * kLinStages * sizeof(uint64_t) + 64 * sizeof(float) + 16;
-  size_t tile_bytes = (size_t)kLinRows * (mt * 8 + 1) * sizeof(float);
-  if (tile_bytes > (size_t)kLinStages * kLinStageBytes) b += tile_bytes;  // never for mt <= 4
+  b += (size_t)mp * (xc + 8) * sizeof(bf16);
+  b += ((size_t)kLinRows * (mp + 1) * sizeof(float) + 15) & ~size_t(15);
+  b += 2 * kLinStages * sizeof(uint64_t) + (kMaxK + 64) * sizeof(float) + 16;
   return b;
+}
+
+void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg) {
+  const long long KB = Kd / kLinBK, T = (long long)n_tiles * KB;
+  const int G = (int)(T < num_sms ? T : num_sms);
+  int ms = 1;
+  for (int t = 0; t < n_tiles; ++t) {
+    const int c0 = (int)(((t * KB + 1) * G - 1) / T);
+    const int c1 = (int)(((t * KB + KB) * G - 1) / T);
+    if (c1 - c0 + 1 > ms) ms = c1 - c0 + 1;
+  }
+  *grid = G;
+  *max_seg = ms;
 }
 
 cudaError_t prepare_linear_kernels() {

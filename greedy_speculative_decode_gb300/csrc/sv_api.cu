@@ -112,21 +112,6 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
   return r == CUDA_SUCCESS;
 }
 
-// Split of the K dimension: a function of the weight shape only, so every
-// row of every call sums its products in the same order.
-int choose_splits(int n_tiles, int Kd) {
-  const int kb = Kd / kLinBK;
-  int last_ok = 1;
-  for (int s = 1; s <= kb; ++s) {
-    if (kb % s) continue;
-    if (Kd / s > kLinKcMax) continue;
-    last_ok = s;
-    if (n_tiles * s >= kLinTargetCtas) return s;
-    if (Kd / s <= 2 * kLinBK) return s;  // do not cut a CTA's share below two k blocks
-  }
-  return last_ok;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int n_tiles, int map) {
@@ -134,8 +119,7 @@ int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int
   d->N = rows;
   d->Kd = Kd;
   d->n_tiles = n_tiles;
-  d->splits = choose_splits(n_tiles, Kd);
-  d->Kc = Kd / d->splits;
+  linear_partition(n_tiles, Kd, ctx->num_sms, &d->grid, &d->max_seg);
   d->map_kind = map;
   if (!make_map(&d->map, w, (uint64_t)rows, (uint64_t)Kd, 64))
     return fail(ctx, SV_E_CUDA, "cuTensorMapEncodeTiled failed for a weight of %d x %d", rows, Kd);
@@ -207,7 +191,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       p.X = ctx->x;
       p.x_ss = ctx->x_ss;
       p.gain = ctx->attn_norm[l];
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
       p.out = ctx->q;
       p.out_stride = Hq * d;
       p.kcache = ctx->kpool + loff;
@@ -223,7 +207,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       LinParams p = base;
       const LinearDesc& ld = ctx->lin_o[l];
       p.X = ctx->o;
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
       p.out = ctx->x;
       p.out_stride = H;
       p.out_ss = ctx->x_ss;
@@ -235,7 +219,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       p.X = ctx->x;
       p.x_ss = ctx->x_ss;
       p.gain = ctx->ffn_norm[l];
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
       p.out = ctx->a;
       p.out_stride = c.ffn;
       CK(launch_linear(ld, p, EPI_GLU, true, s, ctx->use_pdl));
@@ -244,7 +228,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       LinParams p = base;
       const LinearDesc& ld = ctx->lin_down[l];
       p.X = ctx->a;
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
       p.out = ctx->x;
       p.out_stride = H;
       p.out_ss = ctx->x_ss;
@@ -257,7 +241,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
     p.X = ctx->x;
     p.x_ss = ctx->x_ss;
     p.gain = ctx->final_norm;
-    p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.splits = ld.splits; p.Kc = ld.Kc; p.map = ld.map_kind;
+    p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
     p.logits = logits;
     p.logits_row0 = (mode == MODE_PREFILL) ? M - 1 : 0;
     p.am_val = ctx->am_val;
@@ -465,7 +449,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   size_t ws_floats = 0;
   int max_tiles = ctx->lin_head.n_tiles;
   auto acc_ws = [&](const LinearDesc& ld) {
-    if (ld.splits > 1) ws_floats = std::max(ws_floats, (size_t)ld.n_tiles * ld.splits * kLinRows * MP);
+    if (ld.max_seg > 1) ws_floats = std::max(ws_floats, (size_t)ld.n_tiles * ld.max_seg * kLinRows * MP);
     max_tiles = std::max(max_tiles, ld.n_tiles);
   };
   for (int l = 0; l < L; ++l) {
@@ -714,7 +698,7 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
       } else {
         ld = &ctx->lin_head; epi = EPI_LOGITS; norm = true; p.X = ctx->x; p.gain = ctx->final_norm;
       }
-      p.Kd = ld->Kd; p.n_tiles = ld->n_tiles; p.splits = ld->splits; p.Kc = ld->Kc; p.map = ld->map_kind;
+      p.Kd = ld->Kd; p.n_tiles = ld->n_tiles; p.max_seg = ld->max_seg; p.map = ld->map_kind;
       CK(launch_linear(*ld, p, epi, norm, ctx->stream, !(r == 0 && l == 0)));
       if (r == 0) {
         const double n_out = which == SV_LIN_GATE_UP ? (double)c.ffn : (double)ld->N;

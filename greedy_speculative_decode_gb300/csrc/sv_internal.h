@@ -20,11 +20,12 @@ constexpr int kLinRows = 128;
 constexpr int kLinBK = 64;
 constexpr int kLinChunkBytes = 64 * 128;           // one 64 x 64 bf16 box, 128B-swizzled
 constexpr int kLinStageBytes = 2 * kLinChunkBytes;  // both chunks of one k block
-constexpr int kLinStages = 4;
+constexpr int kLinStages = 8;
+// Input columns a CTA stages at once, for 8 padded token rows (half as many
+// for 16, a quarter for 32): 64 KB of shared memory.
+constexpr int kLinXCols = 4096;
 constexpr int kLinConsumerWarps = 8;
 constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;
-constexpr int kLinKcMax = 1024;  // most input columns one CTA stages (bounds its smem)
-constexpr int kLinTargetCtas = 304;
 
 // Attention geometry: a split is 256 absolute positions = 4 warps x 4 pages.
 constexpr int kAttnWarps = 4;
@@ -61,8 +62,8 @@ struct LinParams {
   const bf16* gain;   // [Kd]
   int ss_tiles;
   float eps;
-  int M, Kd, n_tiles, splits, Kc, map, ffn, head_dim;
-  float* ws;     // split-K partial tiles
+  int M, Kd, n_tiles, max_seg, map, ffn, head_dim;
+  float* ws;     // partial tiles of tiles shared by several CTAs: [n_tiles][max_seg][128][MP]
   int* counters; // one ticket per tile
   // epilogue operands
   bf16* out;           // EPI_QKV: q [M, Hq d]; EPI_RESID: x [M, N] (in place); EPI_GLU: a [M, ffn]
@@ -96,16 +97,19 @@ struct AttnParams {
 };
 
 // ------------------------------------------------------------------ launches
+// A weight matrix as the linear kernel streams it: grid = one CTA per SM (at
+// most one per k-block), max_seg = most CTAs any 128-row tile is split over.
 struct LinearDesc {
   CUtensorMap map;
-  int N, Kd, n_tiles, splits, Kc, map_kind;
+  int N, Kd, n_tiles, grid, max_seg, map_kind;
 };
+void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg);
 
 cudaError_t prepare_linear_kernels();
 cudaError_t prepare_attention_kernels();
 cudaError_t launch_linear(const LinearDesc& d, const LinParams& p, int epi, bool norm,
                           cudaStream_t s, bool pdl);
-size_t linear_smem_bytes(int mt, int Kc);
+size_t linear_smem_bytes(int mt);
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
                              int head_dim, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_combine(const AttnParams& p, int head_dim, cudaStream_t s, bool pdl);

@@ -84,21 +84,6 @@ __global__ void __launch_bounds__(256) k_rows_argmax(const float* __restrict__ a
   if (threadIdx.x == 0 && status_out) *status_out = st->status;
 }
 
-// The K split of a weight shape: the same rule the context uses, so this call
-// and the context's LM head sum every product in the same order.
-int splits_for(int n_tiles, int Kd) {
-  const int kb = Kd / kLinBK;
-  int last_ok = 1;
-  for (int s = 1; s <= kb; ++s) {
-    if (kb % s) continue;
-    if (Kd / s > kLinKcMax) continue;
-    last_ok = s;
-    if (n_tiles * s >= kLinTargetCtas) return s;
-    if (Kd / s <= 2 * kLinBK) return s;
-  }
-  return last_ok;
-}
-
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
@@ -118,7 +103,12 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
 
   // Where each piece of scratch goes, and whether it fits.
   const int n_tiles = (vocab + kLinRows - 1) / kLinRows;
-  const int splits = splits_for(n_tiles, hidden);
+  int dev = 0, num_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_E_CUDA;
+  if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SV_E_CUDA;
+  // the same partition of the K dimension as the context's LM head
+  int grid = 1, max_seg = 1;
+  linear_partition(n_tiles, hidden, num_sms, &grid, &max_seg);
   const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const size_t off_state = 0;
   const size_t off_ss = round256(off_state + sizeof(SvState));
@@ -126,11 +116,9 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   const size_t off_amv = round256(off_cnt + sizeof(int) * (size_t)n_tiles);
   const size_t off_ami = round256(off_amv + sizeof(float) * (size_t)M * n_tiles);
   const size_t off_ws = round256(off_ami + sizeof(int) * (size_t)M * n_tiles);
-  const size_t end = off_ws + (splits > 1 ? sizeof(float) * (size_t)n_tiles * splits * kLinRows * mp : 0);
+  const size_t end = off_ws + (max_seg > 1 ? sizeof(float) * (size_t)n_tiles * max_seg * kLinRows * mp : 0);
   if (end > kNoAllocScratchBytes) return SV_E_NOMEM;  // larger than the fixed array
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_E_CUDA;
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     DeviceSetup& ds = g_setup[dev];
@@ -161,8 +149,8 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   d.N = vocab;
   d.Kd = hidden;
   d.n_tiles = n_tiles;
-  d.splits = splits;
-  d.Kc = hidden / splits;
+  d.grid = grid;
+  d.max_seg = max_seg;
   d.map_kind = MAP_PLAIN;
   {
     cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)vocab};
@@ -195,8 +183,7 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   p.M = M;
   p.Kd = hidden;
   p.n_tiles = n_tiles;
-  p.splits = splits;
-  p.Kc = d.Kc;
+  p.max_seg = max_seg;
   p.map = MAP_PLAIN;
   p.ws = ws;
   p.counters = counters;
