@@ -19,289 +19,36 @@
 // G query heads of a group times the rows make one 16-row mma tile.  K and V
 // pages arrive by TMA (128B-swizzled 16 x 64 boxes) into a per-warp ring;
 // Q K^T and P V run on bf16 mma.sync with fp32 accumulation.
-#include "sv_internal.h"
-#include "sv_ptx.cuh"
+#include "attn_dev.cuh"
 
 namespace sv {
 
 namespace {
 
 template <int D>
-struct AttnCfg {
-  static constexpr int kBoxes = D / 64;                // 64-column boxes per page row
-  static constexpr int kPageBytes = kPage * D * 2;     // one K (or V) page of one head
-  static constexpr int kBufBytes = 2 * kPageBytes;     // K + V
-  static constexpr int kBufs = D <= 128 ? 4 : 2;       // pages in flight per warp
-  static constexpr int kQStride = D + 8;               // bf16 elements
-  static constexpr int kRingBytes = kAttnWarps * kBufs * kBufBytes;
-  static constexpr int kQBytes = 16 * kQStride * 2;
-  static constexpr int kScratchBytes = kAttnWarps * 16 * (D + 2) * 4;
-  static constexpr int kSmem = 1024 + (kRingBytes > kScratchBytes ? kRingBytes : kScratchBytes) +
-                               kQBytes + kAttnWarps * kBufs * 8 + 64;
-};
-
-template <int D>
 __global__ void __launch_bounds__(kAttnWarps * 32, 1)
     k_attention(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const AttnParams p) {
-  const int layer = p.layer, max_pages = p.max_pages;
-  using C = AttnCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  constexpr int kRegion = C::kRingBytes > C::kScratchBytes ? C::kRingBytes : C::kScratchBytes;
-  uint8_t* ring = smem;
-  bf16* Qs = reinterpret_cast<bf16*>(smem + kRegion);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRegion + C::kQBytes);
-  float* scratch = reinterpret_cast<float*>(smem);  // aliases the ring after a work item
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, q4 = lane & 3;
-  const int G = p.n_q_heads / p.n_kv_heads;
-  const int RB = kAttnQ / G;  // token rows per work item
-
-  if (tid == 0) {
-    for (int i = 0; i < kAttnWarps * C::kBufs; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
+  AttnSmem<D> sm;
+  sm.carve(smem);
+  if (threadIdx.x == 0) attn_init_bars<D>(sm);
   __syncthreads();
   pdl_trigger();
   pdl_wait();
-
-  const int pos = p.st->step_pos;
-  const int M = p.M;
-  const int n_rb = (M + RB - 1) / RB;
-  const int n_splits = (pos + M + kAttnSplit - 1) / kAttnSplit;
-  const int work = n_splits * p.n_kv_heads * n_rb;
-  uint64_t* my_bars = bars + warp * C::kBufs;
-  uint8_t* my_ring = ring + warp * C::kBufs * C::kBufBytes;
-  uint32_t phase = 0;  // parity bit per buffer of this warp
-  const uint64_t pol = policy_evict_first();
-
-  for (int w = blockIdx.x; w < work; w += gridDim.x) {
-    const int rb = w % n_rb;
-    const int h = (w / n_rb) % p.n_kv_heads;
-    const int split = w / (n_rb * p.n_kv_heads);
-    const int r0 = rb * RB;
-    const int nrows = min(RB, M - r0);
-    const int ctx_max = pos + r0 + nrows;  // largest context of the block's rows
-
-    // ---- Q tile: query qi = (token row r0 + qi / G, head h G + qi % G)
-    for (int v = tid; v < 16 * (D / 8); v += kAttnWarps * 32) {
-      const int qi = v / (D / 8), c8 = v % (D / 8);
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (qi < nrows * G) {
-        const int r = r0 + qi / G, hq = h * G + qi % G;
-        val = *reinterpret_cast<const uint4*>(p.q + (size_t)r * p.n_q_heads * D + hq * D + c8 * 8);
-      }
-      *reinterpret_cast<uint4*>(Qs + qi * C::kQStride + c8 * 8) = val;
-    }
-    __syncthreads();
-
-    // ---- this warp's four pages
-    const int wpos0 = split * kAttnSplit + warp * (kAttnPagesPerWarp * kPage);
-    int npages = 0;
-    while (npages < kAttnPagesPerWarp && wpos0 + npages * kPage < ctx_max) ++npages;
-    int page_id[kAttnPagesPerWarp];
-    for (int j = 0; j < kAttnPagesPerWarp; ++j) {
-      int pg = -1;
-      if (j < npages) {
-        const int lp = (wpos0 + j * kPage) / kPage;
-        pg = p.block_table[lp];
-        if (pg < 0 || pg >= max_pages) pg = -1;
-      }
-      page_id[j] = pg;
-    }
-    auto issue = [&](int j) {
-      const int b = j % C::kBufs;
-      uint8_t* kb = my_ring + b * C::kBufBytes;
-      uint8_t* vb = kb + C::kPageBytes;
-      mbar_arrive_expect_tx(&my_bars[b], C::kBufBytes);
-      const int row0 = ((layer * max_pages + page_id[j]) * p.n_kv_heads + h) * kPage;
-      for (int cb = 0; cb < C::kBoxes; ++cb) {
-        tma_load_2d(kb + cb * 2048, &kmap, cb * 64, row0, &my_bars[b], pol);
-        tma_load_2d(vb + cb * 2048, &vmap, cb * 64, row0, &my_bars[b], pol);
-      }
-    };
-    bool bad = false;
-    for (int j = 0; j < npages; ++j) bad |= page_id[j] < 0;
-    if (bad) {
-      if (lane == 0) atomicOr(&p.st->status, ST_BAD_PAGE);
-      npages = 0;
-    }
-    if (lane == 0)
-      for (int j = 0; j < npages && j < C::kBufs; ++j) issue(j);
-
-    // query rows held by this lane: g and g + 8
-    const int ctx_lo = pos + r0 + g / G + 1;
-    const int ctx_hi = pos + r0 + (g + 8) / G + 1;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.0f, 0.0f};
-    float o[D / 8][4];
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
-
-    const uint32_t q_base = smem_u32(Qs) + (uint32_t)((((lane & 7) + ((lane >> 3) & 1) * 8) * C::kQStride +
-                                                       (lane >> 4) * 8) * 2);
-    bool ok = true;
-    for (int j = 0; j < npages; ++j) {
-      const int b = j % C::kBufs;
-      if (!mbar_wait(&my_bars[b], (phase >> b) & 1u)) {
-        ok = false;
-        break;
-      }
-      phase ^= 1u << b;
-      const uint32_t kb = smem_u32(my_ring + b * C::kBufBytes);
-      const uint32_t vb = kb + C::kPageBytes;
-      // S = Q K^T for 16 queries x 16 positions
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t a[4];
-        ldsm_x4(q_base + kk * 32, a[0], a[1], a[2], a[3]);
-        const int pr = (lane & 7) + ((lane >> 4) & 1) * 8;
-        const int ch = (kk & 3) * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + (kk >> 2) * 2048 + pr * 128 + ((ch ^ (pr & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16(s[0], a, b0, b1);
-        mma_bf16(s[1], a, b2, b3);
-      }
-      // mask (exact -inf beyond each row's context), scale to log2 units
-      const int pbase = wpos0 + j * kPage;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int pabs = pbase + nt * 8 + 2 * q4 + (e & 1);
-          const int ctx = e < 2 ? ctx_lo : ctx_hi;
-          s[nt][e] = pabs < ctx ? __fmul_rn(s[nt][e], p.scale_log2) : -INFINITY;
-        }
-      // online softmax on rows g (e = 0, 1) and g + 8 (e = 2, 3)
-      float alpha[2];
-      uint32_t pa[4];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[rr], mx);
-        float pv[4];
-        if (m_new == -INFINITY) {
-          alpha[rr] = 1.0f;
-          pv[0] = pv[1] = pv[2] = pv[3] = 0.0f;
-        } else {
-          alpha[rr] = exp2f(__fsub_rn(m_run[rr], m_new));
-          pv[0] = bf16r(exp2f(__fsub_rn(s[0][2 * rr], m_new)));
-          pv[1] = bf16r(exp2f(__fsub_rn(s[0][2 * rr + 1], m_new)));
-          pv[2] = bf16r(exp2f(__fsub_rn(s[1][2 * rr], m_new)));
-          pv[3] = bf16r(exp2f(__fsub_rn(s[1][2 * rr + 1], m_new)));
-        }
-        float sum = __fadd_rn(__fadd_rn(pv[0], pv[1]), __fadd_rn(pv[2], pv[3]));
-        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
-        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 2));
-        l_run[rr] = __fadd_rn(__fmul_rn(l_run[rr], alpha[rr]), sum);
-        m_run[rr] = m_new;
-        pa[rr] = pack_bf16x2(pv[0], pv[1]);      // positions 2q, 2q+1
-        pa[2 + rr] = pack_bf16x2(pv[2], pv[3]);  // positions 8+2q, 9+2q
-      }
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] = __fmul_rn(o[n][0], alpha[0]);
-        o[n][1] = __fmul_rn(o[n][1], alpha[0]);
-        o[n][2] = __fmul_rn(o[n][2], alpha[1]);
-        o[n][3] = __fmul_rn(o[n][3], alpha[1]);
-      }
-      // O += P V
-      const uint32_t afr[4] = {pa[0], pa[1], pa[2], pa[3]};
-#pragma unroll
-      for (int dn = 0; dn < D / 16; ++dn) {
-        const int pr = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int ch = ((dn * 16) & 63) / 8 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_trans(vb + ((dn * 16) >> 6) * 2048 + pr * 128 + ((ch ^ (pr & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16(o[2 * dn], afr, b0, b1);
-        mma_bf16(o[2 * dn + 1], afr, b2, b3);
-      }
-      fence_proxy_async_smem();  // reads of buffer b precede its next TMA write
-      __syncwarp();
-      if (lane == 0 && j + C::kBufs < npages) issue(j + C::kBufs);
-    }
-    if (!ok && lane == 0) atomicOr(&p.st->status, ST_TIMEOUT);
-    __syncthreads();  // every warp is done with its ring: reuse it as scratch
-
-    // ---- per-warp partials to scratch: [warp][16][D + 2] (m, l, o[D])
-    float* sw = scratch + warp * 16 * (D + 2);
-    if (q4 == 0) {
-      sw[g * (D + 2)] = m_run[0];
-      sw[g * (D + 2) + 1] = l_run[0];
-      sw[(g + 8) * (D + 2)] = m_run[1];
-      sw[(g + 8) * (D + 2) + 1] = l_run[1];
-    }
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      const int c = n * 8 + 2 * q4;
-      sw[g * (D + 2) + 2 + c] = o[n][0];
-      sw[g * (D + 2) + 3 + c] = o[n][1];
-      sw[(g + 8) * (D + 2) + 2 + c] = o[n][2];
-      sw[(g + 8) * (D + 2) + 3 + c] = o[n][3];
-    }
-    __syncthreads();
-    // ---- merge the warps in order 0..3 and write the split partial
-    const int nq = nrows * G;
-    for (int e = tid; e < nq * (D / 8); e += kAttnWarps * 32) {
-      const int qi = e / (D / 8), c0 = (e % (D / 8)) * 8;
-      float mw[kAttnWarps], mx = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < kAttnWarps; ++ww) {
-        mw[ww] = scratch[(ww * 16 + qi) * (D + 2)];
-        mx = fmaxf(mx, mw[ww]);
-      }
-      float L = 0.0f, acc[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
-      if (mx != -INFINITY) {
-#pragma unroll
-        for (int ww = 0; ww < kAttnWarps; ++ww) {
-          if (mw[ww] == -INFINITY) continue;
-          const float sc = exp2f(__fsub_rn(mw[ww], mx));
-          const float* src = scratch + (ww * 16 + qi) * (D + 2);
-          L = __fadd_rn(L, __fmul_rn(src[1], sc));
-#pragma unroll
-          for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(src[2 + c0 + c], sc));
-        }
-      }
-      const int r = r0 + qi / G, hq = h * G + qi % G;
-      const size_t slot = ((size_t)r * p.n_q_heads + hq) * p.max_splits + split;
-      if (c0 == 0) p.part_ml[slot] = make_float2(mx, L);
-      float* dst = p.part_o + slot * D + c0;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
-    fence_proxy_async_smem();  // scratch (in the ring) is overwritten by TMA next item
-    __syncthreads();            // scratch (= ring) and Qs are rewritten by the next item
-  }
+  uint32_t phase = 0;
+  if (!attn_items<D>(p, &kmap, &vmap, blockIdx.x, gridDim.x, sm, phase) && (threadIdx.x & 31) == 0)
+    atomicOr(&p.st->status, ST_TIMEOUT);
 }
 
-// out[r, hq, :] = merge of the split partials s < ceil((pos + r + 1) / 256), in order.
 template <int D>
 __global__ void __launch_bounds__(D) k_attn_combine(const AttnParams p) {
   pdl_trigger();
   pdl_wait();
-  const int r = blockIdx.x / p.n_q_heads, hq = blockIdx.x % p.n_q_heads;
-  const int i = threadIdx.x;
-  const int ctx = p.st->step_pos + r + 1;
-  const int ns = (ctx + kAttnSplit - 1) / kAttnSplit;
-  const size_t base = ((size_t)r * p.n_q_heads + hq) * p.max_splits;
-  float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, p.part_ml[base + s].x);
-  float L = 0.0f, acc = 0.0f;
-  for (int s = 0; s < ns; ++s) {
-    const float2 ml = p.part_ml[base + s];
-    if (ml.x == -INFINITY) continue;
-    const float sc = exp2f(__fsub_rn(ml.x, mx));
-    L = __fadd_rn(L, __fmul_rn(ml.y, sc));
-    acc = __fadd_rn(acc, __fmul_rn(p.part_o[(base + s) * D + i], sc));
-  }
-  p.out[(size_t)r * p.n_q_heads * D + hq * D + i] = __float2bfloat16_rn(__fdiv_rn(acc, L));
+  combine_element<D>(p, blockIdx.x / p.n_q_heads, blockIdx.x % p.n_q_heads, threadIdx.x,
+                     __ldcg(&p.st->step_pos));
 }
 
 template <int D>

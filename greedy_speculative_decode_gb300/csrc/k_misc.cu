@@ -1,7 +1,6 @@
 // k_misc.cu -- the small kernels of a step: embedding gather, the
 // argmax + accept + truncate kernel, and cache housekeeping.
-#include "sv_internal.h"
-#include "sv_ptx.cuh"
+#include "misc_dev.cuh"
 
 namespace sv {
 
@@ -13,30 +12,13 @@ __global__ void __launch_bounds__(128) k_embed(const bf16* __restrict__ E, int h
                                                bf16* __restrict__ x, float* __restrict__ x_ss,
                                                int ss_tiles, SvState* st) {
   pdl_trigger();
+  __shared__ float part[4];
   const int t = blockIdx.x, m = blockIdx.y, i = threadIdx.x;
   if (t == 0 && m == 0 && i == 0) st->step_pos = st->seq_len;
-  int tok = st->tokens[m];
-  if (tok < 0 || tok >= vocab) {
-    if (i == 0) atomicOr(&st->status, ST_BAD_TOKEN);
-    tok = 0;
-  }
-  const int col = t * 128 + i;
-  const bf16 v = E[(size_t)tok * hidden + col];
-  x[(size_t)m * hidden + col] = v;
-  float f = __bfloat162float(v);
-  float ss = __fmul_rn(f, f);
-  for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-  __shared__ float part[4];
-  if ((i & 31) == 0) part[i >> 5] = ss;
-  __syncthreads();
-  if (i == 0)
-    x_ss[m * ss_tiles + t] = __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
+  embed_tile(E, hidden, vocab, x, x_ss, ss_tiles, st, m, t, i, part, 3);
 }
 
-// Greedy argmax of each row from the LM head's per-tile partials (largest
-// value, lowest id on ties), then acceptance: n = number of leading drafts
-// tokens[j+1] equal to argmax[j]; the row count committed is n + 1; rejected
-// window slots are zeroed in every layer (CTA l zeroes layer l).
+// Acceptance for the whole step; CTA l zeroes the rejected rows of layer l.
 __global__ void __launch_bounds__(256) k_accept(SvState* st, const float* __restrict__ am_val,
                                                 const int* __restrict__ am_idx, int n_tiles, int M,
                                                 int mode, bf16* kpool, bf16* vpool,
@@ -46,73 +28,8 @@ __global__ void __launch_bounds__(256) k_accept(SvState* st, const float* __rest
   pdl_wait();
   __shared__ int s_am[kMaxK];
   __shared__ int s_n;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int pos = st->step_pos;
-  if (mode == MODE_BODY) {
-    if (blockIdx.x == 0 && tid == 0) {
-      st->seq_len = pos + M;
-      st->result[0] = M - 1;
-      st->result[1] = -1;
-      st->result[2] = pos + M;
-      st->result[3] = st->status;
-    }
-    return;
-  }
-  for (int r = warp; r < M; r += 8) {
-    float best = -INFINITY;
-    int bidx = 0x7fffffff;
-    for (int t = lane; t < n_tiles; t += 32) {
-      const float v = am_val[r * n_tiles + t];
-      const int id = am_idx[r * n_tiles + t];
-      if (bidx == 0x7fffffff || v > best || (v == best && id < bidx)) {
-        best = v;
-        bidx = id;
-      }
-    }
-    for (int o = 1; o < 32; o <<= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-      if (oi != 0x7fffffff && (bidx == 0x7fffffff || ov > best || (ov == best && oi < bidx))) {
-        best = ov;
-        bidx = oi;
-      }
-    }
-    if (lane == 0) s_am[r] = bidx;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int n = M - 1;
-    if (mode == MODE_VERIFY) {
-      n = 0;
-      while (n < M - 1 && st->tokens[n + 1] == s_am[n]) ++n;
-    }
-    s_n = n;
-  }
-  __syncthreads();
-  const int n = s_n;
-  const int new_len = pos + 1 + n;
-  if (blockIdx.x == 0 && tid == 0) {
-    for (int r = 0; r < M; ++r) st->argmax[r] = s_am[r];
-    st->seq_len = new_len;
-    st->result[0] = n;
-    st->result[1] = s_am[n];
-    st->result[2] = new_len;
-    st->result[3] = st->status;
-  }
-  // zero the K/V of rejected rows (positions new_len .. pos + M - 1) of layer blockIdx.x
-  const int l = blockIdx.x;
-  if (l >= n_layers) return;
-  const int row = n_kv_heads * head_dim;
-  for (int e = tid; e < (pos + M - new_len) * row; e += blockDim.x) {
-    const int ps = new_len + e / row, hi = e % row;
-    const int page = block_table[ps / kPage];
-    if (page < 0) continue;
-    const int h = hi / head_dim, i = hi % head_dim;
-    const size_t idx = (size_t)l * layer_stride +
-                       (((size_t)page * n_kv_heads + h) * kPage + ps % kPage) * head_dim + i;
-    kpool[idx] = __float2bfloat16_rn(0.0f);
-    vpool[idx] = __float2bfloat16_rn(0.0f);
-  }
+  accept_work(st, am_val, am_idx, n_tiles, M, mode, kpool, vpool, layer_stride, block_table,
+              n_layers, n_kv_heads, head_dim, blockIdx.x, gridDim.x, s_am, &s_n);
 }
 
 // cos/sin of pos * theta^(-2i/d), taken in double and rounded to fp32.

@@ -1,0 +1,554 @@
+// lin_dev.cuh -- the batch-invariant linear: Y[m, n] = sum_k X[m, k] W[n, k]
+// for the few rows m of a decode / verify step, with fused prologue and
+// epilogues.
+//
+// Weights are the only large operand, so the kernel is built to stream them
+// once from HBM at full bandwidth: one producer warp issues TMA loads of
+// 128-row x 64-column weight boxes (128B-swizzled) into an 8-stage mbarrier
+// ring; eight consumer warps feed them to bf16 tensor-core mma.sync with the
+// weight rows as the 16-row A operand and the token rows as the 8-column B
+// operand ("swap AB").  Every output element is the same sequence of mma
+// instructions over the same k order whatever M is (token rows are
+// independent mma columns, padded with zeros to 8, 16 or 32), the split of K
+// over CTAs depends only on the weight shape, and split partials are summed
+// in split order by whichever CTA arrives last.  So row r of an M-row call is
+// bit-identical to the same row computed alone: the requirement of
+// "Phase 23: Speculative Verify Parity" section 2 step 3 (verify rows must
+// round exactly like single-token decode), met here without the page's
+// per-row GEMV, which re-reads every weight once per row.
+//
+// Prologue (norm): X rows are RMS-normalised on the fly from per-128-column
+// partial sums of squares written by the producer of X.
+// Epilogues: QKV (per-head RMSNorm of q and k, rotate-half RoPE, paged K/V
+// write of rows pos..pos+M-1), RESID (residual add in place + new partial
+// sums of squares), GLU (act(gate) * up), LOGITS (bf16 logits + per-tile
+// argmax with ties to the lowest id).
+#pragma once
+#include "sv_internal.h"
+#include "sv_ptx.cuh"
+
+namespace sv {
+namespace {
+
+// A bf16 load that bypasses L1: the data was written by other CTAs (an
+// earlier kernel of the step, or this one), never cached here.
+__device__ __forceinline__ float ldcg_bf16(const bf16* p) {
+  unsigned short u = __ldcg(reinterpret_cast<const unsigned short*>(p));
+  return __uint_as_float((uint32_t)u << 16);
+}
+
+struct TileRows {
+  int a0, b0;  // first weight row of chunk A (local rows 0..63) and chunk B (64..127)
+};
+
+__device__ __forceinline__ TileRows tile_rows_of(int map, int ffn, int tile) {
+  TileRows t;
+  if (map == MAP_GATE_UP) {
+    t.a0 = tile * 64;
+    t.b0 = ffn + tile * 64;
+  } else if (map == MAP_HEAD256) {
+    int h = tile >> 1, j = tile & 1;
+    t.a0 = h * 256 + j * 64;
+    t.b0 = t.a0 + 128;
+  } else {
+    t.a0 = tile * kLinRows;
+    t.b0 = t.a0 + 64;
+  }
+  return t;
+}
+
+__device__ __forceinline__ TileRows tile_rows(const LinParams& p, int tile) {
+  return tile_rows_of(p.map, p.ffn, tile);
+}
+
+__device__ __forceinline__ int local_to_row(const TileRows& t, int lr) {
+  return lr < 64 ? t.a0 + lr : t.b0 + (lr - 64);
+}
+
+__device__ __forceinline__ float act_fn(float g, int act) {
+  if (act == 0) return g / (1.0f + expf(-g));
+  const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+  return 0.5f * g * (1.0f + tanhf(k0 * (g + k1 * g * g * g)));
+}
+
+// QKV epilogue: per-head norm + RoPE + stores.  T: [128][TS] fp32 tile,
+// already summed over splits, columns m < M valid.
+__device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, float* s_rstd) {
+  const int tid = threadIdx.x, M = p.M, d = p.head_dim;
+  const int nthr = kLinConsumerWarps * 32;
+  const TileRows tr = tile_rows(p, tile);
+  const int pos = __ldcg(&p.st->step_pos);
+  const int qrows = p.n_q_heads * d, krows = p.n_kv_heads * d;
+  // 1. round the projection to bf16
+  for (int e = tid; e < kLinRows * M; e += nthr) {
+    int lr = e % kLinRows, m = e / kLinRows;
+    T[lr * TS + m] = bf16r(T[lr * TS + m]);
+  }
+  named_sync(1, nthr);
+  // 2. per-head RMSNorm of q and k (head_dim <= 128: whole heads in the tile)
+  const int heads_in_tile = d <= 128 ? kLinRows / d : 0;
+  const bool tile_qk = local_to_row(tr, 0) < qrows + krows;
+  if (p.q_gain != nullptr && heads_in_tile > 0 && tile_qk) {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int seg = warp; seg < M * heads_in_tile; seg += kLinConsumerWarps) {
+      int m = seg / heads_in_tile, hh = seg % heads_in_tile;
+      float ss = 0.0f;
+      for (int i = lane; i < d; i += 32) {
+        float v = T[(hh * d + i) * TS + m];
+        ss = __fadd_rn(ss, __fmul_rn(v, v));
+      }
+      for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+      if (lane == 0) s_rstd[seg] = 1.0f / sqrtf(ss / (float)d + p.eps);
+    }
+    named_sync(1, nthr);
+    for (int e = tid; e < kLinRows * M; e += nthr) {
+      int lr = e % kLinRows, m = e / kLinRows;
+      int f = local_to_row(tr, lr);
+      if (f >= qrows + krows) continue;
+      const bf16* g = f < qrows ? p.q_gain : p.k_gain;
+      float r = s_rstd[m * heads_in_tile + lr / d];
+      T[lr * TS + m] = bf16r(bf16r(T[lr * TS + m] * r) * __bfloat162float(g[lr % d]));
+    }
+    named_sync(1, nthr);
+  }
+  // 3. RoPE on q and k pairs (i, i + d/2), then the stores
+  const int half = d / 2;
+  for (int e = tid; e < kLinRows * M; e += nthr) {
+    int lr = e % kLinRows, m = e / kLinRows;
+    int f = local_to_row(tr, lr);
+    int i = f % d;
+    int head = f / d;
+    float v = T[lr * TS + m];
+    float outv = v;
+    if (f < qrows + krows) {
+      int lp = (i < half) ? lr + (d <= 128 ? half : 64) : lr - (d <= 128 ? half : 64);
+      float other = T[lp * TS + m];
+      int ii = i < half ? i : i - half;
+      float2 cs = p.rope[(size_t)(pos + m) * half + ii];
+      outv = (i < half) ? __fsub_rn(__fmul_rn(v, cs.x), __fmul_rn(other, cs.y))
+                        : __fadd_rn(__fmul_rn(v, cs.x), __fmul_rn(other, cs.y));
+    }
+    bf16 ob = __float2bfloat16_rn(outv);
+    if (f < qrows) {
+      p.out[(size_t)m * p.out_stride + f] = ob;
+    } else {
+      int kvh = (f < qrows + krows) ? head - p.n_q_heads : head - p.n_q_heads - p.n_kv_heads;
+      int ps = pos + m;
+      int page = (ps < __ldcg(&p.st->cap_len)) ? p.block_table[ps / kPage] : -1;
+      if (page < 0) {
+        atomicOr(&p.st->status, ST_BAD_PAGE);
+        continue;
+      }
+      size_t idx = (((size_t)page * p.n_kv_heads + kvh) * kPage + (ps % kPage)) * d + i;
+      if (f < qrows + krows)
+        p.kcache[idx] = ob;
+      else
+        p.vcache[idx] = ob;
+    }
+  }
+  // the cached K/V are read next through TMA (the async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ void epilogue_resid(const LinParams& p, int tile, float* T, int TS) {
+  const int tid = threadIdx.x, M = p.M, nthr = kLinConsumerWarps * 32;
+  const int n0 = tile * kLinRows;
+  for (int e = tid; e < kLinRows * M; e += nthr) {
+    int lr = e % kLinRows, m = e / kLinRows;
+    size_t o = (size_t)m * p.out_stride + n0 + lr;
+    float r = ldcg_bf16(p.out + o);
+    float v = bf16r(__fadd_rn(r, bf16r(T[lr * TS + m])));
+    p.out[o] = __float2bfloat16_rn(v);
+    T[lr * TS + m] = v;
+  }
+  named_sync(1, nthr);
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int m = warp; m < M; m += kLinConsumerWarps) {
+    float ss = 0.0f;
+    for (int j = 0; j < kLinRows / 32; ++j) {
+      float v = T[(lane + 32 * j) * TS + m];
+      ss = __fadd_rn(ss, __fmul_rn(v, v));
+    }
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    if (lane == 0) p.out_ss[m * p.n_tiles + tile] = ss;
+  }
+  // the next linear reads these rows with bulk copies (the async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ void epilogue_glu(const LinParams& p, int tile, const float* T, int TS) {
+  const int tid = threadIdx.x, M = p.M, nthr = kLinConsumerWarps * 32;
+  for (int e = tid; e < 64 * M; e += nthr) {
+    int lr = e % 64, m = e / 64;
+    float g = bf16r(T[lr * TS + m]);
+    float u = bf16r(T[(lr + 64) * TS + m]);
+    float a = bf16r(act_fn(g, p.act));
+    p.out[(size_t)m * p.out_stride + tile * 64 + lr] = __float2bfloat16_rn(__fmul_rn(a, u));
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // read next by bulk copies
+}
+
+__device__ void epilogue_logits(const LinParams& p, int tile, float* T, int TS) {
+  const int tid = threadIdx.x, M = p.M, nthr = kLinConsumerWarps * 32;
+  const int n0 = tile * kLinRows;
+  for (int e = tid; e < kLinRows * M; e += nthr) {
+    int lr = e % kLinRows, m = e / kLinRows;
+    float v = bf16r(T[lr * TS + m]);
+    T[lr * TS + m] = v;
+    if (p.logits != nullptr && m >= p.logits_row0 && n0 + lr < p.vocab)
+      p.logits[(size_t)(m - p.logits_row0) * p.vocab + n0 + lr] = v;
+  }
+  named_sync(1, nthr);
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int m = warp; m < M; m += kLinConsumerWarps) {
+    // each lane scans 4 consecutive rows in order, then a fixed tree picks the
+    // largest value, the lowest id among equal values
+    float best = -INFINITY;
+    int bidx = 0x7fffffff;
+    for (int j = 0; j < 4; ++j) {
+      int lr = lane * 4 + j;
+      if (n0 + lr >= p.vocab) continue;
+      float v = T[lr * TS + m];
+      if (bidx == 0x7fffffff || v > best) {
+        best = v;
+        bidx = n0 + lr;
+      }
+    }
+    for (int o = 1; o < 32; o <<= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+      if (ov > best || (ov == best && oi < bidx)) {
+        best = ov;
+        bidx = oi;
+      }
+    }
+    if (lane == 0) {
+      p.am_val[m * p.n_tiles + tile] = best;
+      p.am_idx[m * p.n_tiles + tile] = bidx;
+    }
+  }
+}
+
+// Owner of flattened k-block kb under the even split of T k-blocks over G CTAs
+// (CTA c owns [c T / G, (c + 1) T / G)).
+__device__ __forceinline__ int owner_cta(long long kb, long long T, int G) {
+  return (int)(((kb + 1) * G - 1) / T);
+}
+
+// Input staging.  The CTA's input window is columns c0 + t (mod Kd), t in
+// [0, ncols), of the M rows; it is staged XC columns at a time (usually all at
+// once).  One thread bulk-copies each row's run of the chunk into xs (row
+// stride XS) -- two copies where the window wraps past Kd -- so the whole
+// chunk is one L2 round trip; with NORM the rows are then RMS-normalised in
+// place.  Rows M..MP-1 are zero (set before the kernel waits on its
+// predecessor).  c0, t0, XC and Kd are multiples of 64.
+
+// Thread 0: issue the bulk copies of chunk [t0, t0 + nc) of the M rows.
+__device__ __forceinline__ void stage_issue(const LinParams& p, bf16* xs, int XS, int c0, int t0,
+                                            int nc, uint64_t* xbar) {
+  mbar_arrive_expect_tx(xbar, (uint32_t)(p.M * nc * (int)sizeof(bf16)));
+  int k0 = c0 + t0;
+  if (k0 >= p.Kd) k0 -= p.Kd;
+  const int first = min(nc, p.Kd - k0);  // columns before the wrap
+  for (int m = 0; m < p.M; ++m) {
+    const bf16* row = p.X + (size_t)m * p.Kd;
+    bf16* dst = xs + (size_t)m * XS;
+    bulk_load(dst, row + k0, (uint32_t)(first * sizeof(bf16)), xbar);
+    if (first < nc) bulk_load(dst + first, row, (uint32_t)((nc - first) * sizeof(bf16)), xbar);
+  }
+}
+
+// y = bf16(bf16(x * rstd) * gain) of eight bf16 values.
+__device__ __forceinline__ uint4 norm8(uint4 x, float r, uint4 g) {
+  const bf16* xb = reinterpret_cast<const bf16*>(&x);
+  const bf16* gb = reinterpret_cast<const bf16*>(&g);
+  uint32_t w[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float y0 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * q]), r)),
+                                     __bfloat162float(gb[2 * q])));
+    const float y1 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * q + 1]), r)),
+                                     __bfloat162float(gb[2 * q + 1])));
+    w[q] = pack_bf16x2(y0, y1);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Shared-memory carve-up of a linear CTA (see linear_smem_bytes).
+struct LinSmem {
+  uint8_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* xbar;  // completion of the input rows' bulk copies
+  bf16* xs;
+  float* T;
+  float* s_rstd;   // [kMaxK] row rstd of the input
+  float* s_hrstd;  // [64] per-head rstd (QKV epilogue)
+  int* s_flag;
+};
+
+template <int MT>
+__device__ __forceinline__ LinSmem lin_smem(uint8_t* smem) {
+  constexpr int MP = MT * 8, TS = MP + 1, XS = kLinXCols / MT + 8;
+  LinSmem sm;
+  sm.ring = smem;
+  sm.xs = reinterpret_cast<bf16*>(smem + kLinStages * kLinStageBytes);
+  sm.T = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sm.xs) + MP * XS * sizeof(bf16));
+  sm.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm.T) +
+                                        ((kLinRows * TS * sizeof(float) + 15) & ~size_t(15)));
+  sm.empty = sm.full + kLinStages;
+  sm.xbar = sm.empty + kLinStages;
+  sm.s_rstd = reinterpret_cast<float*>(sm.xbar + 1);
+  sm.s_hrstd = sm.s_rstd + kMaxK;
+  sm.s_flag = reinterpret_cast<int*>(sm.s_hrstd + 64);
+  return sm;
+}
+
+// k-block range [kb_begin, kb_end) of CTA `cta` of G over the flattened
+// n_tiles x (Kd/64) blocks.
+__device__ __forceinline__ void lin_range(const LinParams& p, int cta, int G, long long& kb_begin,
+                                          long long& kb_end) {
+  const long long Tk = (long long)p.n_tiles * (p.Kd / kLinBK);
+  kb_begin = (long long)cta * Tk / G;
+  kb_end = (long long)(cta + 1) * Tk / G;
+}
+
+// Producer (one thread): TMA the CTA's weight boxes into the ring.  `it`
+// counts ring uses (stage = it mod stages, parity = its quotient's low bit),
+// kept in step with the consumers'.  Returns false on a timeout.
+__device__ bool lin_produce(const LinParams& p, const CUtensorMap* wmap, int cta, int G,
+                            const LinSmem& sm, int& it, uint64_t pol) {
+  const int KB = p.Kd / kLinBK;
+  long long kb_begin, kb_end;
+  lin_range(p, cta, G, kb_begin, kb_end);
+  int tile = (int)(kb_begin / KB), kk = (int)(kb_begin % KB);  // walked without division
+  for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
+    const int s = it % kLinStages;
+    if (it >= kLinStages && !mbar_wait(&sm.empty[s], ((it / kLinStages) & 1) ^ 1)) return false;
+    const TileRows tr = tile_rows(p, tile);
+    mbar_arrive_expect_tx(&sm.full[s], kLinStageBytes);
+    uint8_t* dst = sm.ring + s * kLinStageBytes;
+    tma_load_2d(dst, wmap, kk * kLinBK, tr.a0, &sm.full[s], pol);
+    tma_load_2d(dst + kLinChunkBytes, wmap, kk * kLinBK, tr.b0, &sm.full[s], pol);
+    if (++kk == KB) {
+      kk = 0;
+      ++tile;
+    }
+  }
+  return true;
+}
+
+// Producer, after its own stream: prefetch into L2 the first pf_blocks
+// k-blocks that CTA `cta` streams in the next linear of the step.
+__device__ void lin_prefetch_next(const LinParams& p, const CUtensorMap* pfmap, int cta) {
+  if (p.pf_blocks <= 0 || cta >= p.pf_grid) return;
+  const int KB = p.pf_Kd / kLinBK;
+  const long long Tk = (long long)p.pf_n_tiles * KB;
+  const long long b0 = (long long)cta * Tk / p.pf_grid;
+  long long b1 = (long long)(cta + 1) * Tk / p.pf_grid;
+  if (b1 > b0 + p.pf_blocks) b1 = b0 + p.pf_blocks;
+  int tile = (int)(b0 / KB), kk = (int)(b0 % KB);
+  for (long long kb = b0; kb < b1; ++kb) {
+    const TileRows tr = tile_rows_of(p.pf_map, p.pf_ffn, tile);
+    tma_prefetch_l2(pfmap, kk * kLinBK, tr.a0);
+    tma_prefetch_l2(pfmap, kk * kLinBK, tr.b0);
+    if (++kk == KB) {
+      kk = 0;
+      ++tile;
+    }
+  }
+}
+
+// Consumers (the kLinConsumerWarps warps, named barrier 1): multiply the
+// CTA's share of the weight with the staged input rows and finish every tile
+// that ends in this CTA.  Returns false if a stage never arrived.
+template <int MT, int EPI, bool NORM>
+__device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& sm, int& it) {
+  constexpr int MP = MT * 8;          // padded token rows
+  constexpr int TS = MP + 1;          // epilogue tile row stride
+  constexpr int XC = kLinXCols / MT;  // input columns staged at once
+  constexpr int XS = XC + 8;          // staged row stride in elements (16B pad: no bank conflicts)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nthr = kLinConsumerWarps * 32;
+  const int KB = p.Kd / kLinBK;
+  const long long Tk = (long long)p.n_tiles * KB;
+  long long kb_begin, kb_end;
+  lin_range(p, cta, G, kb_begin, kb_end);
+  if (kb_begin >= kb_end) return true;
+  float* T = sm.T;
+  constexpr int VPR = XC / 8;                        // 16-byte vectors per staged row
+  constexpr int CPT = (VPR + kLinConsumerWarps * 32 - 1) / (kLinConsumerWarps * 32);
+  const int c0 = (int)(kb_begin % KB) * kLinBK;
+  const int ncols = (int)((kb_end - kb_begin) * kLinBK < p.Kd ? (kb_end - kb_begin) * kLinBK : p.Kd);
+
+  // ---- before the wait on the previous kernel: nothing here depends on it
+  for (int v = tid; v < (MP - p.M) * (XS / 8); v += nthr)  // padding rows are zero
+    reinterpret_cast<uint4*>(sm.xs + (size_t)p.M * XS)[v] = make_uint4(0u, 0u, 0u, 0u);
+  uint4 gain0[CPT];  // gain of this thread's column vectors of the first chunk
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    gain0[j] = make_uint4(0u, 0u, 0u, 0u);
+    const int c8 = tid + j * nthr;
+    if (NORM && c8 < VPR && c8 * 8 < ncols) {
+      int k = c0 + c8 * 8;
+      if (k >= p.Kd) k -= p.Kd;
+      gain0[j] = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
+    }
+  }
+  pdl_wait();  // X, its sums of squares and the step state come from earlier kernels
+
+  const int chunk = warp >> 2, rg = warp & 3;
+  const int g = lane >> 2, q = lane & 3;
+  const int lr0 = chunk * 64 + rg * 16 + g;
+  const int a_row = rg * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);  // row within the 64-row chunk
+  const int a_khalf = lane >> 4;
+  const uint32_t xs_base =
+      smem_u32(sm.xs) + (uint32_t)(((lane & 7) * XS + ((lane >> 3) & 1) * 8) * sizeof(bf16));
+  float acc[MT][4];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+
+  bool ok = true;
+  int staged = -1;
+  uint32_t xphase = 0;
+  long long seg_begin = kb_begin;
+  int tile_c = (int)(kb_begin / KB), kk_c = (int)(kb_begin % KB);  // walked without division
+  for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
+    const int tile = tile_c, kk = kk_c;
+    if (++kk_c == KB) {
+      kk_c = 0;
+      ++tile_c;
+    }
+    int jw = kk * kLinBK - c0;  // column offset within the window
+    if (jw < 0) jw += p.Kd;
+    const int xchunk = jw / XC;
+    if (xchunk != staged) {
+      const int t0 = xchunk * XC, nc = min(XC, ncols - t0);
+      fence_proxy_async_smem();  // earlier reads and writes of xs precede the bulk copies
+      named_sync(1, nthr);
+      if (tid == 0) stage_issue(p, sm.xs, XS, c0, t0, nc, sm.xbar);
+      if (NORM && staged < 0) {  // row rstd, one warp per row, while the copies fly
+        for (int m = warp; m < p.M; m += kLinConsumerWarps) {
+          float ss = 0.0f;
+          for (int t = lane; t < p.ss_tiles; t += 32) ss = __fadd_rn(ss, __ldcg(p.x_ss + m * p.ss_tiles + t));
+          for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+          if (lane == 0) sm.s_rstd[m] = 1.0f / sqrtf(ss / (float)p.Kd + p.eps);
+        }
+        named_sync(1, nthr);
+      }
+      if (!mbar_wait(sm.xbar, xphase)) ok = false;
+      xphase ^= 1u;
+      if (NORM) {
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const int c8 = tid + j * nthr;
+          if (c8 >= VPR || c8 * 8 >= nc) continue;
+          uint4 gv = gain0[j];
+          if (staged >= 0) {  // a later chunk: its own gain columns
+            int k = c0 + t0 + c8 * 8;
+            if (k >= p.Kd) k -= p.Kd;
+            gv = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
+          }
+          for (int m = 0; m < p.M; ++m) {
+            uint4* ptr = reinterpret_cast<uint4*>(sm.xs + (size_t)m * XS + c8 * 8);
+            *ptr = norm8(*ptr, sm.s_rstd[m], gv);
+          }
+        }
+      }
+      named_sync(1, nthr);
+      staged = xchunk;
+    }
+    const int s = it % kLinStages;
+    if (ok && !mbar_wait(&sm.full[s], (it / kLinStages) & 1)) ok = false;
+    if (ok) {
+      const uint32_t tile_base = smem_u32(sm.ring + s * kLinStageBytes + chunk * kLinChunkBytes);
+      const uint32_t xcol = (uint32_t)(jw - xchunk * XC);
+#pragma unroll
+      for (int k16 = 0; k16 < kLinBK / 16; ++k16) {
+        uint32_t a[4];
+        const int kc = k16 * 2 + a_khalf;
+        ldsm_x4(tile_base + a_row * 128 + ((kc ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          uint32_t b0, b1;
+          ldsm_x2(xs_base + (uint32_t)(((t * 8) * XS + xcol + k16 * 16) * sizeof(bf16)), b0, b1);
+          mma_bf16(acc[t], a, b0, b1);
+        }
+      }
+    }
+    fence_proxy_async_smem();  // our ldmatrix reads of stage s precede its next TMA write
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+
+    if (kk != KB - 1 && kb != kb_end - 1) continue;
+    // ------------ this CTA's part of `tile` is complete
+    const int kk_first = kk - (int)(kb - seg_begin);
+    seg_begin = kb + 1;
+    named_sync(1, nthr);  // the previous tile's epilogue is done with T
+    if (kk_first == 0 && kk == KB - 1) {
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int m0 = t * 8 + 2 * q;
+        T[lr0 * TS + m0] = acc[t][0];
+        T[lr0 * TS + m0 + 1] = acc[t][1];
+        T[(lr0 + 8) * TS + m0] = acc[t][2];
+        T[(lr0 + 8) * TS + m0 + 1] = acc[t][3];
+      }
+    } else {
+      const int c_first = owner_cta((long long)tile * KB, Tk, G);
+      const int c_last = owner_cta((long long)tile * KB + KB - 1, Tk, G);
+      const int nseg = c_last - c_first + 1, seg = cta - c_first;
+      float* wsb = p.ws + ((size_t)(tile * p.max_seg + seg) * kLinRows) * MP;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int m0 = t * 8 + 2 * q;
+        *reinterpret_cast<float2*>(wsb + lr0 * MP + m0) = make_float2(acc[t][0], acc[t][1]);
+        *reinterpret_cast<float2*>(wsb + (lr0 + 8) * MP + m0) = make_float2(acc[t][2], acc[t][3]);
+      }
+      named_sync(1, nthr);
+      if (tid == 0) {  // publish the CTA's partial (the fence covers the barrier before it)
+        __threadfence();
+        const int prev = atomicAdd(&p.counters[tile], 1);
+        *sm.s_flag = (prev == nseg - 1);
+        __threadfence();
+      }
+      named_sync(1, nthr);
+      const bool last = *sm.s_flag != 0;
+      if (last) {
+        // last CTA of this tile: sum the partials of its CTAs in k order
+        const float* wst = p.ws + ((size_t)tile * p.max_seg * kLinRows) * MP;
+        for (int e = tid; e < kLinRows * p.M; e += nthr) {
+          const int lr = e / p.M, m = e % p.M;
+          float part[kLinMaxSeg];
+#pragma unroll
+          for (int j = 0; j < kLinMaxSeg; ++j)
+            if (j < nseg) part[j] = __ldcg(wst + ((size_t)j * kLinRows + lr) * MP + m);
+          float v = part[0];
+#pragma unroll
+          for (int j = 1; j < kLinMaxSeg; ++j)
+            if (j < nseg) v = __fadd_rn(v, part[j]);
+          T[lr * TS + m] = v;
+        }
+        if (tid == 0) p.counters[tile] = 0;  // ready for the next use
+      }
+#pragma unroll
+      for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+      if (!last) continue;
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    named_sync(1, nthr);
+    if (EPI == EPI_QKV)
+      epilogue_qkv(p, tile, T, TS, sm.s_hrstd);
+    else if (EPI == EPI_RESID)
+      epilogue_resid(p, tile, T, TS);
+    else if (EPI == EPI_GLU)
+      epilogue_glu(p, tile, T, TS);
+    else
+      epilogue_logits(p, tile, T, TS);
+  }
+  return ok;
+}
+
+}  // namespace
+}  // namespace sv

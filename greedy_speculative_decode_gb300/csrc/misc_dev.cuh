@@ -1,0 +1,114 @@
+// misc_dev.cuh -- the small pieces of a step as device functions: the embedding gather
+// (with the row statistics the first RMSNorm needs) and the argmax +
+// acceptance + truncation of the window.
+#pragma once
+#include "sv_internal.h"
+#include "sv_ptx.cuh"
+
+namespace sv {
+namespace {
+
+// x[m, 128t + i] = E[token_m, 128t + i] for i < 128 threads of one group
+// (named barrier `bar`), and x_ss[m, t] = the tile's sum of squares.
+__device__ __forceinline__ void embed_tile(const bf16* __restrict__ E, int hidden, int vocab,
+                                           bf16* __restrict__ x, float* __restrict__ x_ss,
+                                           int ss_tiles, SvState* st, int m, int t, int i,
+                                           float* part, int bar) {
+  int tok = st->tokens[m];
+  if (tok < 0 || tok >= vocab) {
+    if (i == 0) atomicOr(&st->status, ST_BAD_TOKEN);
+    tok = 0;
+  }
+  const int col = t * 128 + i;
+  const bf16 v = E[(size_t)tok * hidden + col];
+  x[(size_t)m * hidden + col] = v;
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // x is read next by bulk copies
+  float f = __bfloat162float(v);
+  float ss = __fmul_rn(f, f);
+  for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+  if ((i & 31) == 0) part[i >> 5] = ss;
+  named_sync(bar, 128);
+  if (i == 0)
+    x_ss[m * ss_tiles + t] = __fadd_rn(__fadd_rn(part[0], part[1]), __fadd_rn(part[2], part[3]));
+  named_sync(bar, 128);  // part is reused by the group's next tile
+}
+
+// Greedy argmax of each row from the LM head's per-tile partials (largest
+// value, lowest id on ties), then acceptance: n = number of leading drafts
+// tokens[j+1] equal to argmax[j]; the row count committed is n + 1.  CTA 0
+// writes the results; the K/V of rejected rows are zeroed in layers
+// cta, cta + G_ctas, ...  Runs on 256 threads (named barrier 1).
+__device__ void accept_work(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
+                            int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
+                            const int* block_table, int n_layers, int n_kv_heads, int head_dim,
+                            int cta, int G_ctas, int* s_am, int* s_n) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int pos = __ldcg(&st->step_pos);
+  if (mode == MODE_BODY) {
+    if (cta == 0 && tid == 0) {
+      st->seq_len = pos + M;
+      st->result[0] = M - 1;
+      st->result[1] = -1;
+      st->result[2] = pos + M;
+      st->result[3] = st->status;
+    }
+    return;
+  }
+  for (int r = warp; r < M; r += 8) {
+    float best = -INFINITY;
+    int bidx = 0x7fffffff;
+    for (int t = lane; t < n_tiles; t += 32) {
+      const float v = __ldcg(&am_val[r * n_tiles + t]);
+      const int id = __ldcg(&am_idx[r * n_tiles + t]);
+      if (bidx == 0x7fffffff || v > best || (v == best && id < bidx)) {
+        best = v;
+        bidx = id;
+      }
+    }
+    for (int o = 1; o < 32; o <<= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+      if (oi != 0x7fffffff && (bidx == 0x7fffffff || ov > best || (ov == best && oi < bidx))) {
+        best = ov;
+        bidx = oi;
+      }
+    }
+    if (lane == 0) s_am[r] = bidx;
+  }
+  named_sync(1, 256);
+  if (tid == 0) {
+    int n = M - 1;
+    if (mode == MODE_VERIFY) {
+      n = 0;
+      while (n < M - 1 && st->tokens[n + 1] == s_am[n]) ++n;
+    }
+    *s_n = n;
+  }
+  named_sync(1, 256);
+  const int n = *s_n;
+  const int new_len = pos + 1 + n;
+  if (cta == 0 && tid == 0) {
+    for (int r = 0; r < M; ++r) st->argmax[r] = s_am[r];
+    st->seq_len = new_len;
+    st->result[0] = n;
+    st->result[1] = s_am[n];
+    st->result[2] = new_len;
+    st->result[3] = st->status;
+  }
+  const int row = n_kv_heads * head_dim;
+  for (int l = cta; l < n_layers; l += G_ctas) {
+    for (int e = tid; e < (pos + M - new_len) * row; e += 256) {
+      const int ps = new_len + e / row, hi = e % row;
+      const int page = block_table[ps / kPage];
+      if (page < 0) continue;
+      const int h = hi / head_dim, i = hi % head_dim;
+      const size_t idx = (size_t)l * layer_stride +
+                         (((size_t)page * n_kv_heads + h) * kPage + ps % kPage) * head_dim + i;
+      kpool[idx] = __float2bfloat16_rn(0.0f);
+      vpool[idx] = __float2bfloat16_rn(0.0f);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace sv

@@ -28,6 +28,7 @@ struct sv_ctx {
   cudaEvent_t ev = nullptr;
   bool use_graphs = true;
   bool use_pdl = true;  // chain a step's kernels with programmatic dependent launch
+  bool use_prefetch = false;  // each linear prefetches the start of the next one into L2
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
   std::vector<const bf16*> attn_norm, q_norm, k_norm, ffn_norm;
@@ -120,6 +121,9 @@ int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int
   d->Kd = Kd;
   d->n_tiles = n_tiles;
   linear_partition(n_tiles, Kd, ctx->num_sms, &d->grid, &d->max_seg);
+  if (d->max_seg > kLinMaxSeg)
+    return fail(ctx, SV_E_INVAL, "weight of %d x %d is split over %d CTAs per tile (max %d)", rows, Kd,
+                d->max_seg, kLinMaxSeg);
   d->map_kind = map;
   if (!make_map(&d->map, w, (uint64_t)rows, (uint64_t)Kd, 64))
     return fail(ctx, SV_E_CUDA, "cuTensorMapEncodeTiled failed for a weight of %d x %d", rows, Kd);
@@ -143,29 +147,90 @@ int dalloc(sv_ctx* ctx, T** p, size_t count) {
 int mp_of(int M) { return M <= 8 ? 8 : (M <= 16 ? 16 : 32); }
 
 // ------------------------------------------------------------------ the step
-// Enqueue every kernel of one step of M rows on ctx->stream.
-int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
+enum LinWhich { LIN_QKV = 0, LIN_O = 1, LIN_GU = 2, LIN_DOWN = 3, LIN_HEAD = 4 };
+
+// Parameters of one linear of one step of M rows.
+LinParams lin_params(sv_ctx* ctx, int which, int l, int M, int mode, float* logits, int* epi,
+                     bool* norm, const LinearDesc** desc) {
   const sv_config& c = ctx->cfg;
-  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
-  cudaStream_t s = ctx->stream;
-  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, s));
+  const int H = c.hidden, d = c.head_dim, Hq = c.n_q_heads;
+  LinParams p = {};
+  p.ss_tiles = H / 128;
+  p.eps = c.rms_eps;
+  p.M = M;
+  p.ffn = c.ffn;
+  p.head_dim = d;
+  p.ws = ctx->ws;
+  p.counters = ctx->counters;
+  p.block_table = ctx->block_table;
+  p.rope = ctx->rope;
+  p.n_q_heads = Hq;
+  p.n_kv_heads = c.n_kv_heads;
+  p.act = c.act;
+  p.vocab = c.vocab;
+  p.st = ctx->st;
+  const LinearDesc* ld = nullptr;
+  if (which == LIN_QKV) {
+    ld = &ctx->lin_qkv[l];
+    *epi = EPI_QKV;
+    *norm = true;
+    p.X = ctx->x;
+    p.x_ss = ctx->x_ss;
+    p.gain = ctx->attn_norm[l];
+    p.out = ctx->q;
+    p.out_stride = Hq * d;
+    p.kcache = ctx->kpool + (size_t)l * ctx->layer_stride;
+    p.vcache = ctx->vpool + (size_t)l * ctx->layer_stride;
+    p.q_gain = c.qk_norm ? ctx->q_norm[l] : nullptr;
+    p.k_gain = c.qk_norm ? ctx->k_norm[l] : nullptr;
+  } else if (which == LIN_O) {
+    ld = &ctx->lin_o[l];
+    *epi = EPI_RESID;
+    *norm = false;
+    p.X = ctx->o;
+    p.out = ctx->x;
+    p.out_stride = H;
+    p.out_ss = ctx->x_ss;
+  } else if (which == LIN_GU) {
+    ld = &ctx->lin_gu[l];
+    *epi = EPI_GLU;
+    *norm = true;
+    p.X = ctx->x;
+    p.x_ss = ctx->x_ss;
+    p.gain = ctx->ffn_norm[l];
+    p.out = ctx->a;
+    p.out_stride = c.ffn;
+  } else if (which == LIN_DOWN) {
+    ld = &ctx->lin_down[l];
+    *epi = EPI_RESID;
+    *norm = false;
+    p.X = ctx->a;
+    p.out = ctx->x;
+    p.out_stride = H;
+    p.out_ss = ctx->x_ss;
+  } else {
+    ld = &ctx->lin_head;
+    *epi = EPI_LOGITS;
+    *norm = true;
+    p.X = ctx->x;
+    p.x_ss = ctx->x_ss;
+    p.gain = ctx->final_norm;
+    p.logits = logits;
+    p.logits_row0 = (mode == MODE_PREFILL) ? M - 1 : 0;
+    p.am_val = ctx->am_val;
+    p.am_idx = ctx->am_idx;
+  }
+  p.Kd = ld->Kd;
+  p.n_tiles = ld->n_tiles;
+  p.max_seg = ld->max_seg;
+  p.map = ld->map_kind;
+  p.grid = ld->grid;
+  *desc = ld;
+  return p;
+}
 
-  LinParams base = {};
-  base.ss_tiles = H / 128;
-  base.eps = c.rms_eps;
-  base.M = M;
-  base.ffn = c.ffn;
-  base.head_dim = d;
-  base.ws = ctx->ws;
-  base.counters = ctx->counters;
-  base.block_table = ctx->block_table;
-  base.rope = ctx->rope;
-  base.n_q_heads = Hq;
-  base.n_kv_heads = Hkv;
-  base.act = c.act;
-  base.vocab = c.vocab;
-  base.st = ctx->st;
-
+AttnParams attn_params(sv_ctx* ctx, int l, int M) {
+  const sv_config& c = ctx->cfg;
   AttnParams ap = {};
   ap.q = ctx->q;
   ap.block_table = ctx->block_table;
@@ -174,82 +239,60 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   ap.part_o = ctx->part_o;
   ap.out = ctx->o;
   ap.M = M;
-  ap.n_q_heads = Hq;
-  ap.n_kv_heads = Hkv;
+  ap.n_q_heads = c.n_q_heads;
+  ap.n_kv_heads = c.n_kv_heads;
   ap.max_splits = ctx->max_splits;
   ap.max_pages = c.max_pages;
-  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d));
-  const int G = Hq / Hkv;
+  ap.layer = l;
+  ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
+  return ap;
+}
+
+// Enqueue every kernel of one step of M rows on ctx->stream.
+int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
+  const sv_config& c = ctx->cfg;
+  const int H = c.hidden, d = c.head_dim, Hkv = c.n_kv_heads;
+  cudaStream_t s = ctx->stream;
+  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, s));
+  const int G = c.n_q_heads / Hkv;
   const int n_rb = (M + kAttnQ / G - 1) / (kAttnQ / G);
   const int attn_grid = std::max(1, std::min(ctx->max_splits * Hkv * n_rb, ctx->num_sms));
-
-  for (int l = 0; l < c.n_layers; ++l) {
-    const size_t loff = (size_t)l * ctx->layer_stride;
-    {  // RMSNorm + QKV + QK-norm + RoPE + paged K/V write
-      LinParams p = base;
-      const LinearDesc& ld = ctx->lin_qkv[l];
-      p.X = ctx->x;
-      p.x_ss = ctx->x_ss;
-      p.gain = ctx->attn_norm[l];
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
-      p.out = ctx->q;
-      p.out_stride = Hq * d;
-      p.kcache = ctx->kpool + loff;
-      p.vcache = ctx->vpool + loff;
-      p.q_gain = c.qk_norm ? ctx->q_norm[l] : nullptr;
-      p.k_gain = c.qk_norm ? ctx->k_norm[l] : nullptr;
-      CK(launch_linear(ld, p, EPI_QKV, true, s, ctx->use_pdl));
+  int epi;
+  bool norm;
+  const LinearDesc* ld;
+  // the weight each linear prefetches into L2: the next one of the step (the
+  // last one's next is the first of the following step)
+  const bool head = mode != MODE_BODY;
+  auto next_of = [&](int which, int l) -> const LinearDesc* {
+    if (!ctx->use_prefetch) return nullptr;
+    switch (which) {
+      case LIN_QKV: return &ctx->lin_o[l];
+      case LIN_O: return &ctx->lin_gu[l];
+      case LIN_GU: return &ctx->lin_down[l];
+      case LIN_DOWN:
+        if (l + 1 < c.n_layers) return &ctx->lin_qkv[l + 1];
+        return head ? &ctx->lin_head : &ctx->lin_qkv[0];
+      default: return c.n_layers > 0 ? &ctx->lin_qkv[0] : nullptr;
     }
-    ap.layer = l;
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
+    CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_QKV, l)));
+    AttnParams ap = attn_params(ctx, l, M);
     CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, s, ctx->use_pdl));
     CK(launch_attn_combine(ap, d, s, ctx->use_pdl));
-    {  // attention projection + residual
-      LinParams p = base;
-      const LinearDesc& ld = ctx->lin_o[l];
-      p.X = ctx->o;
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
-      p.out = ctx->x;
-      p.out_stride = H;
-      p.out_ss = ctx->x_ss;
-      CK(launch_linear(ld, p, EPI_RESID, false, s, ctx->use_pdl));
-    }
-    {  // RMSNorm + gate|up + activation
-      LinParams p = base;
-      const LinearDesc& ld = ctx->lin_gu[l];
-      p.X = ctx->x;
-      p.x_ss = ctx->x_ss;
-      p.gain = ctx->ffn_norm[l];
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
-      p.out = ctx->a;
-      p.out_stride = c.ffn;
-      CK(launch_linear(ld, p, EPI_GLU, true, s, ctx->use_pdl));
-    }
-    {  // down projection + residual
-      LinParams p = base;
-      const LinearDesc& ld = ctx->lin_down[l];
-      p.X = ctx->a;
-      p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
-      p.out = ctx->x;
-      p.out_stride = H;
-      p.out_ss = ctx->x_ss;
-      CK(launch_linear(ld, p, EPI_RESID, false, s, ctx->use_pdl));
+    for (int w : {LIN_O, LIN_GU, LIN_DOWN}) {
+      p = lin_params(ctx, w, l, M, mode, logits, &epi, &norm, &ld);
+      CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(w, l)));
     }
   }
-  if (mode != MODE_BODY) {  // final RMSNorm + LM head + per-tile argmax
-    LinParams p = base;
-    const LinearDesc& ld = ctx->lin_head;
-    p.X = ctx->x;
-    p.x_ss = ctx->x_ss;
-    p.gain = ctx->final_norm;
-    p.Kd = ld.Kd; p.n_tiles = ld.n_tiles; p.max_seg = ld.max_seg; p.map = ld.map_kind;
-    p.logits = logits;
-    p.logits_row0 = (mode == MODE_PREFILL) ? M - 1 : 0;
-    p.am_val = ctx->am_val;
-    p.am_idx = ctx->am_idx;
-    CK(launch_linear(ld, p, EPI_LOGITS, true, s, ctx->use_pdl));
+  if (head) {  // final RMSNorm + LM head + per-tile argmax
+    LinParams p = lin_params(ctx, LIN_HEAD, 0, M, mode, logits, &epi, &norm, &ld);
+    CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_HEAD, 0)));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
-                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s, ctx->use_pdl));
+                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s,
+                   ctx->use_pdl));
   return SV_OK;
 }
 
@@ -405,6 +448,10 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   ctx->use_graphs = !(ng && ng[0] == '1');
   const char* np = getenv("SV_NO_PDL");
   ctx->use_pdl = !(np && np[0] == '1');
+  // Off by default: on the 8B-shaped verify step it measured 2 % slower (the
+  // prefetches compete with the slowest CTAs of the current launch).
+  const char* pf = getenv("SV_L2_PREFETCH");
+  ctx->use_prefetch = pf && pf[0] == '1';
   if (prepare_linear_kernels() != cudaSuccess || prepare_attention_kernels() != cudaSuccess)
     return bail(SV_E_CUDA);
 
@@ -699,7 +746,15 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
         ld = &ctx->lin_head; epi = EPI_LOGITS; norm = true; p.X = ctx->x; p.gain = ctx->final_norm;
       }
       p.Kd = ld->Kd; p.n_tiles = ld->n_tiles; p.max_seg = ld->max_seg; p.map = ld->map_kind;
-      CK(launch_linear(*ld, p, epi, norm, ctx->stream, !(r == 0 && l == 0)));
+      p.grid = ld->grid;
+      // the same class of the next layer is prefetched, as much as inside a step
+      const LinearDesc* next = nullptr;
+      if (ctx->use_prefetch && which != SV_LIN_LM_HEAD) {
+        const int ln = (l + 1) % c.n_layers;
+        next = which == SV_LIN_O ? &ctx->lin_o[ln]
+                                 : (which == SV_LIN_GATE_UP ? &ctx->lin_gu[ln] : &ctx->lin_down[ln]);
+      }
+      CK(launch_linear(*ld, p, epi, norm, ctx->stream, !(r == 0 && l == 0), next));
       if (r == 0) {
         const double n_out = which == SV_LIN_GATE_UP ? (double)c.ffn : (double)ld->N;
         bytes += 2.0 * ld->N * ld->Kd + 2.0 * K * ld->Kd + 2.0 * K * n_out;

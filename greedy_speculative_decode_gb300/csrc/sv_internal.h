@@ -24,6 +24,15 @@ constexpr int kLinStages = 8;
 // Input columns a CTA stages at once, for 8 padded token rows (half as many
 // for 16, a quarter for 32): 64 KB of shared memory.
 constexpr int kLinXCols = 4096;
+// Fewest k-blocks (16 KB of weight each) a CTA streams: small matrices use
+// fewer CTAs rather than split tiles into many tiny partial sums.
+constexpr int kLinMinShare = 4;
+// Most CTAs one 128-row tile may be divided over (checked when a weight is set up).
+constexpr int kLinMaxSeg = 16;
+// k-blocks of the next linear each CTA prefetches into L2: 256 KB per CTA,
+// about 39 MB over a full grid of a GB300, some 6 us of HBM time -- about the
+// gap a launch boundary leaves.
+constexpr int kLinPrefetchBlocks = 16;
 constexpr int kLinConsumerWarps = 8;
 constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;
 
@@ -63,6 +72,7 @@ struct LinParams {
   int ss_tiles;
   float eps;
   int M, Kd, n_tiles, max_seg, map, ffn, head_dim;
+  int grid;      // CTAs the weight is divided over (one per SM, at most one per k-block)
   float* ws;     // partial tiles of tiles shared by several CTAs: [n_tiles][max_seg][128][MP]
   int* counters; // one ticket per tile
   // epilogue operands
@@ -82,6 +92,11 @@ struct LinParams {
   int* am_idx;
   int vocab;
   SvState* st;
+  // L2 prefetch: once the producer has issued its own stream, it prefetches
+  // the first pf_blocks k-blocks that the CTA of the same index streams in the
+  // next linear of the step (that weight's tensor map is the kernel's second
+  // parameter), so the next launch starts from L2 instead of a cold HBM ramp.
+  int pf_blocks, pf_n_tiles, pf_Kd, pf_grid, pf_map, pf_ffn;
 };
 
 struct AttnParams {
@@ -108,7 +123,7 @@ void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg)
 cudaError_t prepare_linear_kernels();
 cudaError_t prepare_attention_kernels();
 cudaError_t launch_linear(const LinearDesc& d, const LinParams& p, int epi, bool norm,
-                          cudaStream_t s, bool pdl);
+                          cudaStream_t s, bool pdl, const LinearDesc* next = nullptr);
 size_t linear_smem_bytes(int mt);
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
                              int head_dim, int grid, cudaStream_t s, bool pdl);

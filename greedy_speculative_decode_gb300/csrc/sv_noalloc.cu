@@ -109,6 +109,7 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   // the same partition of the K dimension as the context's LM head
   int grid = 1, max_seg = 1;
   linear_partition(n_tiles, hidden, num_sms, &grid, &max_seg);
+  if (max_seg > kLinMaxSeg) return SV_E_INVAL;
   const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const size_t off_state = 0;
   const size_t off_ss = round256(off_state + sizeof(SvState));
@@ -184,6 +185,7 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   p.Kd = hidden;
   p.n_tiles = n_tiles;
   p.max_seg = max_seg;
+  p.grid = grid;
   p.map = MAP_PLAIN;
   p.ws = ws;
   p.counters = counters;
