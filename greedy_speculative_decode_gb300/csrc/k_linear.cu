@@ -49,6 +49,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
       mbar_init(&sm.empty[s], kLinConsumerWarps);
     }
     mbar_init(sm.xbar, 1);
+    mbar_init(sm.gbar, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -128,7 +129,8 @@ size_t linear_smem_bytes(int mt) {
   b += (size_t)kLinStages * kLinStageBytes;
   b += (size_t)mp * (xc + 8) * sizeof(bf16);
   b += ((size_t)kLinRows * (mp + 1) * sizeof(float) + 15) & ~size_t(15);
-  b += (2 * kLinStages + 1) * sizeof(uint64_t) + (kMaxK + 64) * sizeof(float) + 16;
+  b += (size_t)xc * sizeof(bf16);  // gain window
+  b += (2 * kLinStages + 2) * sizeof(uint64_t) + (kMaxK + 64) * sizeof(float) + 16;
   return b;
 }
 

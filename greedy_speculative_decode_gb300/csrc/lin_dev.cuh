@@ -71,13 +71,58 @@ __device__ __forceinline__ float act_fn(float g, int act) {
   return 0.5f * g * (1.0f + tanhf(k0 * (g + k1 * g * g * g)));
 }
 
+// Epilogue operands that live in global memory, loaded for a tile as soon as
+// the CTA has finished its share of it -- before it learns whether it is the
+// CTA that completes the tile -- so their latency overlaps the exchange of
+// partial sums.  Element j of thread tid is e = tid + j * 256: row lr = e mod
+// 128 of the tile, token row m = e / 128 (the epilogues' own order).
+template <int MP>
+struct EpiPre {
+  static constexpr int N = (kLinRows * MP + kLinConsumerWarps * 32 - 1) / (kLinConsumerWarps * 32);
+  float res[N];   // EPI_RESID: the residual x[m, n0 + lr]
+  float2 cs[N];   // EPI_QKV: (cos, sin) of the element's RoPE angle
+  int page[N];    // EPI_QKV: physical page of position pos + m (-1: none)
+};
+
+template <int MP, int EPI>
+__device__ __forceinline__ void epi_preload(const LinParams& p, int tile, int pos, int cap,
+                                            EpiPre<MP>& pre) {
+  const int tid = threadIdx.x, nthr = kLinConsumerWarps * 32;
+  if (EPI == EPI_RESID) {
+#pragma unroll
+    for (int j = 0; j < EpiPre<MP>::N; ++j) {
+      const int e = tid + j * nthr;
+      if (e < kLinRows * p.M)
+        pre.res[j] = ldcg_bf16(p.out + (size_t)(e / kLinRows) * p.out_stride + tile * kLinRows + e % kLinRows);
+    }
+  } else if (EPI == EPI_QKV) {
+    const TileRows tr = tile_rows(p, tile);
+    const int d = p.head_dim, half = d / 2;
+    const int qrows = p.n_q_heads * d, krows = p.n_kv_heads * d;
+#pragma unroll
+    for (int j = 0; j < EpiPre<MP>::N; ++j) {
+      const int e = tid + j * nthr;
+      pre.cs[j] = make_float2(1.0f, 0.0f);
+      pre.page[j] = -1;
+      if (e < kLinRows * p.M) {
+        const int lr = e % kLinRows, m = e / kLinRows;
+        const int f = local_to_row(tr, lr), i = f % d;
+        if (f < qrows + krows) pre.cs[j] = p.rope[(size_t)(pos + m) * half + (i < half ? i : i - half)];
+        const int ps = pos + m;
+        if (f >= qrows && ps < cap) pre.page[j] = p.block_table[ps / kPage];
+      }
+    }
+  }
+}
+
 // QKV epilogue: per-head norm + RoPE + stores.  T: [128][TS] fp32 tile,
 // already summed over splits, columns m < M valid.
-__device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, float* s_rstd) {
+template <int MP>
+__device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, float* s_rstd, int pos,
+                             const EpiPre<MP>& pre) {
   const int tid = threadIdx.x, M = p.M, d = p.head_dim;
   const int nthr = kLinConsumerWarps * 32;
   const TileRows tr = tile_rows(p, tile);
-  const int pos = __ldcg(&p.st->step_pos);
   const int qrows = p.n_q_heads * d, krows = p.n_kv_heads * d;
   // 1. round the projection to bf16
   for (int e = tid; e < kLinRows * M; e += nthr) {
@@ -113,7 +158,10 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
   }
   // 3. RoPE on q and k pairs (i, i + d/2), then the stores
   const int half = d / 2;
-  for (int e = tid; e < kLinRows * M; e += nthr) {
+#pragma unroll
+  for (int j = 0; j < EpiPre<MP>::N; ++j) {
+    const int e = tid + j * nthr;
+    if (e >= kLinRows * M) break;
     int lr = e % kLinRows, m = e / kLinRows;
     int f = local_to_row(tr, lr);
     int i = f % d;
@@ -123,8 +171,7 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
     if (f < qrows + krows) {
       int lp = (i < half) ? lr + (d <= 128 ? half : 64) : lr - (d <= 128 ? half : 64);
       float other = T[lp * TS + m];
-      int ii = i < half ? i : i - half;
-      float2 cs = p.rope[(size_t)(pos + m) * half + ii];
+      const float2 cs = pre.cs[j];
       outv = (i < half) ? __fsub_rn(__fmul_rn(v, cs.x), __fmul_rn(other, cs.y))
                         : __fadd_rn(__fmul_rn(v, cs.x), __fmul_rn(other, cs.y));
     }
@@ -133,8 +180,8 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
       p.out[(size_t)m * p.out_stride + f] = ob;
     } else {
       int kvh = (f < qrows + krows) ? head - p.n_q_heads : head - p.n_q_heads - p.n_kv_heads;
-      int ps = pos + m;
-      int page = (ps < __ldcg(&p.st->cap_len)) ? p.block_table[ps / kPage] : -1;
+      const int ps = pos + m;
+      const int page = pre.page[j];
       if (page < 0) {
         atomicOr(&p.st->status, ST_BAD_PAGE);
         continue;
@@ -150,14 +197,17 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__device__ void epilogue_resid(const LinParams& p, int tile, float* T, int TS) {
+template <int MP>
+__device__ void epilogue_resid(const LinParams& p, int tile, float* T, int TS, const EpiPre<MP>& pre) {
   const int tid = threadIdx.x, M = p.M, nthr = kLinConsumerWarps * 32;
   const int n0 = tile * kLinRows;
-  for (int e = tid; e < kLinRows * M; e += nthr) {
+#pragma unroll
+  for (int j = 0; j < EpiPre<MP>::N; ++j) {
+    const int e = tid + j * nthr;
+    if (e >= kLinRows * M) break;
     int lr = e % kLinRows, m = e / kLinRows;
     size_t o = (size_t)m * p.out_stride + n0 + lr;
-    float r = ldcg_bf16(p.out + o);
-    float v = bf16r(__fadd_rn(r, bf16r(T[lr * TS + m])));
+    float v = bf16r(__fadd_rn(pre.res[j], bf16r(T[lr * TS + m])));
     p.out[o] = __float2bfloat16_rn(v);
     T[lr * TS + m] = v;
   }
@@ -258,20 +308,18 @@ __device__ __forceinline__ void stage_issue(const LinParams& p, bf16* xs, int XS
   }
 }
 
-// y = bf16(bf16(x * rstd) * gain) of eight bf16 values.
+// y = bf16(bf16(x * rstd) * gain) of two packed bf16 values (low half first).
+__device__ __forceinline__ uint32_t norm2(uint32_t x2, float r, uint32_t g2) {
+  const float x0 = __uint_as_float(x2 << 16), x1 = __uint_as_float(x2 & 0xffff0000u);
+  const uint32_t t2 = pack_bf16x2(__fmul_rn(x0, r), __fmul_rn(x1, r));
+  const float t0 = __uint_as_float(t2 << 16), t1 = __uint_as_float(t2 & 0xffff0000u);
+  const float g0 = __uint_as_float(g2 << 16), g1 = __uint_as_float(g2 & 0xffff0000u);
+  return pack_bf16x2(__fmul_rn(t0, g0), __fmul_rn(t1, g1));
+}
+
+// The same for eight values.
 __device__ __forceinline__ uint4 norm8(uint4 x, float r, uint4 g) {
-  const bf16* xb = reinterpret_cast<const bf16*>(&x);
-  const bf16* gb = reinterpret_cast<const bf16*>(&g);
-  uint32_t w[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float y0 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * q]), r)),
-                                     __bfloat162float(gb[2 * q])));
-    const float y1 = bf16r(__fmul_rn(bf16r(__fmul_rn(__bfloat162float(xb[2 * q + 1]), r)),
-                                     __bfloat162float(gb[2 * q + 1])));
-    w[q] = pack_bf16x2(y0, y1);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  return make_uint4(norm2(x.x, r, g.x), norm2(x.y, r, g.y), norm2(x.z, r, g.z), norm2(x.w, r, g.w));
 }
 
 // Shared-memory carve-up of a linear CTA (see linear_smem_bytes).
@@ -280,8 +328,10 @@ struct LinSmem {
   uint64_t* full;
   uint64_t* empty;
   uint64_t* xbar;  // completion of the input rows' bulk copies
+  uint64_t* gbar;  // completion of the gain window's bulk copy
   bf16* xs;
   float* T;
+  bf16* gs;        // gain of the input window (NORM)
   float* s_rstd;   // [kMaxK] row rstd of the input
   float* s_hrstd;  // [64] per-head rstd (QKV epilogue)
   int* s_flag;
@@ -289,16 +339,18 @@ struct LinSmem {
 
 template <int MT>
 __device__ __forceinline__ LinSmem lin_smem(uint8_t* smem) {
-  constexpr int MP = MT * 8, TS = MP + 1, XS = kLinXCols / MT + 8;
+  constexpr int MP = MT * 8, TS = MP + 1, XC = kLinXCols / MT, XS = XC + 8;
   LinSmem sm;
   sm.ring = smem;
   sm.xs = reinterpret_cast<bf16*>(smem + kLinStages * kLinStageBytes);
   sm.T = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sm.xs) + MP * XS * sizeof(bf16));
-  sm.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm.T) +
-                                        ((kLinRows * TS * sizeof(float) + 15) & ~size_t(15)));
+  sm.gs = reinterpret_cast<bf16*>(reinterpret_cast<uint8_t*>(sm.T) +
+                                  ((kLinRows * TS * sizeof(float) + 15) & ~size_t(15)));
+  sm.full = reinterpret_cast<uint64_t*>(sm.gs + XC);
   sm.empty = sm.full + kLinStages;
   sm.xbar = sm.empty + kLinStages;
-  sm.s_rstd = reinterpret_cast<float*>(sm.xbar + 1);
+  sm.gbar = sm.xbar + 1;
+  sm.s_rstd = reinterpret_cast<float*>(sm.gbar + 1);
   sm.s_hrstd = sm.s_rstd + kMaxK;
   sm.s_flag = reinterpret_cast<int*>(sm.s_hrstd + 64);
   return sm;
@@ -359,6 +411,29 @@ __device__ void lin_prefetch_next(const LinParams& p, const CUtensorMap* pfmap, 
   }
 }
 
+// The input window of CTA `cta`: columns c0 + t (mod Kd), t < ncols.
+__device__ __forceinline__ void lin_window(const LinParams& p, long long kb_begin, long long kb_end,
+                                           int& c0, int& ncols) {
+  const int KB = p.Kd / kLinBK;
+  c0 = (int)(kb_begin % KB) * kLinBK;
+  const long long n = (kb_end - kb_begin) * kLinBK;
+  ncols = (int)(n < p.Kd ? n : p.Kd);
+}
+
+// Normalise in place the 16-byte vectors v = first + tid, first + tid + 256,
+// ... < last of the staged window (vector v: row v / per_row, column vector
+// c8_0 + v % per_row), one or two per thread.
+template <int XS>
+__device__ __forceinline__ void norm_vectors(const LinSmem& sm, int c8_0, int per_row, int nv, int tid,
+                                             int nthr) {
+  const uint4* gs = reinterpret_cast<const uint4*>(sm.gs);
+  for (int v = tid; v < nv; v += nthr) {
+    const int m = v / per_row, c8 = c8_0 + v % per_row;
+    uint4* ptr = reinterpret_cast<uint4*>(sm.xs + (size_t)m * XS + c8 * 8);
+    *ptr = norm8(*ptr, sm.s_rstd[m], gs[c8]);
+  }
+}
+
 // Consumers (the kLinConsumerWarps warps, named barrier 1): multiply the
 // CTA's share of the weight with the staged input rows and finish every tile
 // that ends in this CTA.  Returns false if a stage never arrived.
@@ -376,26 +451,50 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
   lin_range(p, cta, G, kb_begin, kb_end);
   if (kb_begin >= kb_end) return true;
   float* T = sm.T;
-  constexpr int VPR = XC / 8;                        // 16-byte vectors per staged row
-  constexpr int CPT = (VPR + kLinConsumerWarps * 32 - 1) / (kLinConsumerWarps * 32);
-  const int c0 = (int)(kb_begin % KB) * kLinBK;
-  const int ncols = (int)((kb_end - kb_begin) * kLinBK < p.Kd ? (kb_end - kb_begin) * kLinBK : p.Kd);
+  int c0, ncols;
+  lin_window(p, kb_begin, kb_end, c0, ncols);
+  // A window that fits xs is staged once, right after the wait below; with
+  // NORM it is normalised 256 columns (a group) at a time: group 0 before the
+  // main loop, group g + 1 by all consumers while they stream group g, so
+  // only the first group's normalisation is on the critical path.
+  const bool one_chunk = ncols <= XC;
+  constexpr int kGroup = 4 * kLinBK;  // columns per normalisation group
+  const int ngroups = (ncols + kGroup - 1) / kGroup;
 
   // ---- before the wait on the previous kernel: nothing here depends on it
-  for (int v = tid; v < (MP - p.M) * (XS / 8); v += nthr)  // padding rows are zero
+  if (NORM && one_chunk && tid == 0) {  // the gain window
+    const int first = min(ncols, p.Kd - c0);
+    mbar_arrive_expect_tx(sm.gbar, (uint32_t)(ncols * sizeof(bf16)));
+    bulk_load(sm.gs, p.gain + c0, (uint32_t)(first * sizeof(bf16)), sm.gbar);
+    if (first < ncols) bulk_load(sm.gs + first, p.gain, (uint32_t)((ncols - first) * sizeof(bf16)), sm.gbar);
+  }
+  for (int v = tid; v < (MP - p.M) * (XS / 8); v += nthr)  // the padding rows are zero
     reinterpret_cast<uint4*>(sm.xs + (size_t)p.M * XS)[v] = make_uint4(0u, 0u, 0u, 0u);
-  uint4 gain0[CPT];  // gain of this thread's column vectors of the first chunk
-#pragma unroll
-  for (int j = 0; j < CPT; ++j) {
-    gain0[j] = make_uint4(0u, 0u, 0u, 0u);
-    const int c8 = tid + j * nthr;
-    if (NORM && c8 < VPR && c8 * 8 < ncols) {
-      int k = c0 + c8 * 8;
-      if (k >= p.Kd) k -= p.Kd;
-      gain0[j] = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
+  pdl_wait();  // X, its sums of squares and the step state come from earlier kernels
+  if (one_chunk && tid == 0) stage_issue(p, sm.xs, XS, c0, 0, ncols, sm.xbar);
+  int pos = 0, cap = 0;
+  if (EPI == EPI_QKV) {
+    pos = __ldcg(&p.st->step_pos);
+    cap = __ldcg(&p.st->cap_len);
+  }
+  bool ok = true;
+  if (one_chunk) {
+    if (NORM) {  // row rstd (one warp per row) while the copies fly, then group 0
+      for (int m = warp; m < p.M; m += kLinConsumerWarps) {
+        float ss = 0.0f;
+        for (int t = lane; t < p.ss_tiles; t += 32) ss = __fadd_rn(ss, __ldcg(p.x_ss + m * p.ss_tiles + t));
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        if (lane == 0) sm.s_rstd[m] = 1.0f / sqrtf(ss / (float)p.Kd + p.eps);
+      }
+      named_sync(1, nthr);
+      if (!mbar_wait(sm.xbar, 0) || !mbar_wait(sm.gbar, 0)) ok = false;
+      const int w0 = min(kGroup, ncols) / 8;
+      norm_vectors<XS>(sm, 0, w0, p.M * w0, tid, nthr);
+    } else {
+      if (!mbar_wait(sm.xbar, 0)) ok = false;
     }
   }
-  pdl_wait();  // X, its sums of squares and the step state come from earlier kernels
+  named_sync(1, nthr);  // every warp reads every row (padding, group 0)
 
   const int chunk = warp >> 2, rg = warp & 3;
   const int g = lane >> 2, q = lane & 3;
@@ -407,9 +506,10 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
   float acc[MT][4];
 #pragma unroll
   for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+  EpiPre<MP> pre;
 
-  bool ok = true;
-  int staged = -1;
+  int staged = one_chunk ? 0 : -1;  // chunk in xs
+  int normed = 1;                    // groups normalised (one-chunk NORM windows)
   uint32_t xphase = 0;
   long long seg_begin = kb_begin;
   int tile_c = (int)(kb_begin / KB), kk_c = (int)(kb_begin % KB);  // walked without division
@@ -421,8 +521,20 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
     }
     int jw = kk * kLinBK - c0;  // column offset within the window
     if (jw < 0) jw += p.Kd;
-    const int xchunk = jw / XC;
-    if (xchunk != staged) {
+    const int xchunk = one_chunk ? 0 : jw / XC;
+    if (NORM && one_chunk && normed < ngroups && jw == (normed - 1) * kGroup) {
+      // first block of group normed - 1 (first pass over the window): group
+      // normed - 1 is complete everywhere after this barrier; normalise the next
+      named_sync(1, nthr);
+      const int c8_0 = normed * (kGroup / 8);
+      const int w = min(kGroup, ncols - normed * kGroup) / 8;
+      norm_vectors<XS>(sm, c8_0, w, p.M * w, tid, nthr);
+      ++normed;
+    } else if (NORM && one_chunk && normed == ngroups && jw == (normed - 1) * kGroup && ngroups > 1) {
+      named_sync(1, nthr);  // the last group is complete everywhere
+      ++normed;
+    }
+    if (!one_chunk && xchunk != staged) {  // a window of several chunks, staged here chunk by chunk
       const int t0 = xchunk * XC, nc = min(XC, ncols - t0);
       fence_proxy_async_smem();  // earlier reads and writes of xs precede the bulk copies
       named_sync(1, nthr);
@@ -439,16 +551,10 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
       if (!mbar_wait(sm.xbar, xphase)) ok = false;
       xphase ^= 1u;
       if (NORM) {
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const int c8 = tid + j * nthr;
-          if (c8 >= VPR || c8 * 8 >= nc) continue;
-          uint4 gv = gain0[j];
-          if (staged >= 0) {  // a later chunk: its own gain columns
-            int k = c0 + t0 + c8 * 8;
-            if (k >= p.Kd) k -= p.Kd;
-            gv = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
-          }
+        for (int c8 = tid; c8 * 8 < nc; c8 += nthr) {
+          int k = c0 + t0 + c8 * 8;
+          if (k >= p.Kd) k -= p.Kd;
+          const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
           for (int m = 0; m < p.M; ++m) {
             uint4* ptr = reinterpret_cast<uint4*>(sm.xs + (size_t)m * XS + c8 * 8);
             *ptr = norm8(*ptr, sm.s_rstd[m], gv);
@@ -482,6 +588,7 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
 
     if (kk != KB - 1 && kb != kb_end - 1) continue;
     // ------------ this CTA's part of `tile` is complete
+    epi_preload<MP, EPI>(p, tile, pos, cap, pre);
     const int kk_first = kk - (int)(kb - seg_begin);
     seg_begin = kb + 1;
     named_sync(1, nthr);  // the previous tile's epilogue is done with T
@@ -506,11 +613,16 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
         *reinterpret_cast<float2*>(wsb + (lr0 + 8) * MP + m0) = make_float2(acc[t][2], acc[t][3]);
       }
       named_sync(1, nthr);
-      if (tid == 0) {  // publish the CTA's partial (the fence covers the barrier before it)
-        __threadfence();
-        const int prev = atomicAdd(&p.counters[tile], 1);
-        *sm.s_flag = (prev == nseg - 1);
-        __threadfence();
+      if (tid == 0) {
+        // one acq_rel ticket: releases this CTA's partial (the barrier before
+        // it makes the other threads' stores part of it) and acquires those
+        // of the CTAs that arrived before
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(reinterpret_cast<unsigned*>(p.counters + tile))
+                     : "memory");
+        *sm.s_flag = (prev == (unsigned)(nseg - 1));
       }
       named_sync(1, nthr);
       const bool last = *sm.s_flag != 0;
@@ -539,9 +651,9 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
     for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
     named_sync(1, nthr);
     if (EPI == EPI_QKV)
-      epilogue_qkv(p, tile, T, TS, sm.s_hrstd);
+      epilogue_qkv<MP>(p, tile, T, TS, sm.s_hrstd, pos, pre);
     else if (EPI == EPI_RESID)
-      epilogue_resid(p, tile, T, TS);
+      epilogue_resid<MP>(p, tile, T, TS, pre);
     else if (EPI == EPI_GLU)
       epilogue_glu(p, tile, T, TS);
     else

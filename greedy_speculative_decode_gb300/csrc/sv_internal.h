@@ -34,7 +34,7 @@ constexpr int kLinMaxSeg = 16;
 // gap a launch boundary leaves.
 constexpr int kLinPrefetchBlocks = 16;
 constexpr int kLinConsumerWarps = 8;
-constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;
+constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;  // consumers, then the TMA producer
 
 // Attention geometry: a split is 256 absolute positions = 4 warps x 4 pages.
 constexpr int kAttnWarps = 4;
