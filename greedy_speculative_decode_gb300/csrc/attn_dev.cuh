@@ -72,11 +72,15 @@ __device__ __forceinline__ void attn_init_bars(const AttnSmem<D>& sm) {
 
 // Work items w = cta, cta + G_ctas, ... of this step's attention, run by
 // warps 0..kAttnWarps-1 (named barrier 2).  `phase` holds each buffer's
-// parity and persists across calls.  Returns false if a page never arrived.
+// parity.  `pos` is the committed length, final for the whole step: the
+// pages of the first item that hold only positions < pos (written by earlier
+// steps) are requested before the wait on the previous kernel; Q and the page
+// with the step's own rows after it.  Each item writes its split partial (m,
+// l, o), merged by the combine kernel.  Returns false if a page never arrived.
 template <int D>
 __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
                            const CUtensorMap* vmap_p, int cta, int G_ctas, const AttnSmem<D>& sm,
-                           uint32_t& phase) {
+                           uint32_t& phase, int pos) {
   using C = AttnCfg<D>;
   const CUtensorMap& kmap = *kmap_p;
   const CUtensorMap& vmap = *vmap_p;
@@ -89,7 +93,6 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
   const int g = lane >> 2, q4 = lane & 3;
   const int G = p.n_q_heads / p.n_kv_heads;
   const int RB = kAttnQ / G;  // token rows per work item
-  const int pos = __ldcg(&p.st->step_pos);
   const int M = p.M;
   const int n_rb = (M + RB - 1) / RB;
   const int n_splits = (pos + M + kAttnSplit - 1) / kAttnSplit;
@@ -98,6 +101,11 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
   uint8_t* my_ring = ring + warp * C::kBufs * C::kBufBytes;
   const uint64_t pol = policy_evict_first();
   bool all_ok = true;
+  bool waited = false;
+  if (cta >= work) {  // nothing to do: wait only so that the grid completes in order
+    pdl_wait();
+    return true;
+  }
 
   for (int w = cta; w < work; w += G_ctas) {
     const int rb = w % n_rb;
@@ -106,18 +114,6 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
     const int r0 = rb * RB;
     const int nrows = min(RB, M - r0);
     const int ctx_max = pos + r0 + nrows;  // largest context of the block's rows
-
-    // ---- Q tile: query qi = (token row r0 + qi / G, head h G + qi % G)
-    for (int v = tid; v < 16 * (D / 8); v += kAttnWarps * 32) {
-      const int qi = v / (D / 8), c8 = v % (D / 8);
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (qi < nrows * G) {
-        const int r = r0 + qi / G, hq = h * G + qi % G;
-        val = __ldcg(reinterpret_cast<const uint4*>(p.q + (size_t)r * p.n_q_heads * D + hq * D + c8 * 8));
-      }
-      *reinterpret_cast<uint4*>(Qs + qi * C::kQStride + c8 * 8) = val;
-    }
-    named_sync(2, kAttnWarps * 32);
 
     // ---- this warp's four pages
     const int wpos0 = split * kAttnSplit + warp * (kAttnPagesPerWarp * kPage);
@@ -150,10 +146,30 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       if (lane == 0) atomicOr(&p.st->status, ST_BAD_PAGE);
       npages = 0;
     }
+    // pages of positions < pos only: written by earlier steps, requested now
+    int n_old = 0;
+    while (n_old < npages && n_old < C::kBufs && wpos0 + (n_old + 1) * kPage <= pos) ++n_old;
+    if (lane == 0)
+      for (int j = 0; j < n_old; ++j) issue(j);
+    if (!waited) {
+      pdl_wait();  // Q and the K/V of the step's own rows come from the QKV kernel
+      waited = true;
+    }
     if (lane == 0) {
       asm volatile("fence.proxy.async.global;" ::: "memory");  // K/V written with plain stores
-      for (int j = 0; j < npages && j < C::kBufs; ++j) issue(j);
+      for (int j = n_old; j < npages && j < C::kBufs; ++j) issue(j);
     }
+    // ---- Q tile: query qi = (token row r0 + qi / G, head h G + qi % G)
+    for (int v = tid; v < 16 * (D / 8); v += kAttnWarps * 32) {
+      const int qi = v / (D / 8), c8 = v % (D / 8);
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (qi < nrows * G) {
+        const int r = r0 + qi / G, hq = h * G + qi % G;
+        val = __ldcg(reinterpret_cast<const uint4*>(p.q + (size_t)r * p.n_q_heads * D + hq * D + c8 * 8));
+      }
+      *reinterpret_cast<uint4*>(Qs + qi * C::kQStride + c8 * 8) = val;
+    }
+    named_sync(2, kAttnWarps * 32);
 
     // query rows held by this lane: g and g + 8
     const int ctx_lo = pos + r0 + g / G + 1;

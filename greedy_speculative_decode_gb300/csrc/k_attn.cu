@@ -37,9 +37,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32, 1)
   if (threadIdx.x == 0) attn_init_bars<D>(sm);
   __syncthreads();
   pdl_trigger();
-  pdl_wait();
+  // The committed length is final for the whole step (only the step's last
+  // kernel, or the host between steps, changes it), so it may be read before
+  // the wait on the previous kernel; attn_items waits once it has requested
+  // the cache pages that earlier steps wrote.
+  const int pos = __ldcg(&p.st->seq_len);
   uint32_t phase = 0;
-  if (!attn_items<D>(p, &kmap, &vmap, blockIdx.x, gridDim.x, sm, phase) && (threadIdx.x & 31) == 0)
+  if (!attn_items<D>(p, &kmap, &vmap, blockIdx.x, gridDim.x, sm, phase, pos) && (threadIdx.x & 31) == 0)
     atomicOr(&p.st->status, ST_TIMEOUT);
 }
 
