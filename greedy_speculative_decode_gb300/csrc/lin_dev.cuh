@@ -508,89 +508,94 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
   for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
   EpiPre<MP> pre;
 
+  static_assert((kLinStages & (kLinStages - 1)) == 0, "the ring index is taken with a mask");
+  const int Kd = p.Kd;
   int staged = one_chunk ? 0 : -1;  // chunk in xs
-  int normed = 1;                    // groups normalised (one-chunk NORM windows)
   uint32_t xphase = 0;
-  long long seg_begin = kb_begin;
-  int tile_c = (int)(kb_begin / KB), kk_c = (int)(kb_begin % KB);  // walked without division
-  for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
-    const int tile = tile_c, kk = kk_c;
-    if (++kk_c == KB) {
-      kk_c = 0;
-      ++tile_c;
-    }
-    int jw = kk * kLinBK - c0;  // column offset within the window
-    if (jw < 0) jw += p.Kd;
-    const int xchunk = one_chunk ? 0 : jw / XC;
-    if (NORM && one_chunk && normed < ngroups && jw == (normed - 1) * kGroup) {
-      // first block of group normed - 1 (first pass over the window): group
-      // normed - 1 is complete everywhere after this barrier; normalise the next
-      named_sync(1, nthr);
-      const int c8_0 = normed * (kGroup / 8);
-      const int w = min(kGroup, ncols - normed * kGroup) / 8;
-      norm_vectors<XS>(sm, c8_0, w, p.M * w, tid, nthr);
-      ++normed;
-    } else if (NORM && one_chunk && normed == ngroups && jw == (normed - 1) * kGroup && ngroups > 1) {
-      named_sync(1, nthr);  // the last group is complete everywhere
-      ++normed;
-    }
-    if (!one_chunk && xchunk != staged) {  // a window of several chunks, staged here chunk by chunk
-      const int t0 = xchunk * XC, nc = min(XC, ncols - t0);
-      fence_proxy_async_smem();  // earlier reads and writes of xs precede the bulk copies
-      named_sync(1, nthr);
-      if (tid == 0) stage_issue(p, sm.xs, XS, c0, t0, nc, sm.xbar);
-      if (NORM && staged < 0) {  // row rstd, one warp per row, while the copies fly
-        for (int m = warp; m < p.M; m += kLinConsumerWarps) {
-          float ss = 0.0f;
-          for (int t = lane; t < p.ss_tiles; t += 32) ss = __fadd_rn(ss, __ldcg(p.x_ss + m * p.ss_tiles + t));
-          for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-          if (lane == 0) sm.s_rstd[m] = 1.0f / sqrtf(ss / (float)p.Kd + p.eps);
-        }
+  // one-chunk NORM windows: at the first block of group g (window column
+  // g * kGroup, g < ngroups) the consumers sync -- group g is then complete
+  // everywhere -- and normalise group g + 1; norm_at is the next such column
+  int norm_next = 1;
+  int norm_at = (NORM && one_chunk && ngroups > 1) ? 0 : -1;
+  int tile = (int)(kb_begin / KB), kk0 = (int)(kb_begin % KB);
+  long long left = kb_end - kb_begin;
+  int jw = 0;  // window column of the next k-block
+  while (left > 0) {
+    const int nblk = (int)(left < KB - kk0 ? left : KB - kk0);  // k-blocks of `tile` in this CTA
+    for (int j = 0; j < nblk; ++j, ++it) {
+      if (NORM && jw == norm_at) {
         named_sync(1, nthr);
+        if (norm_next < ngroups) {
+          const int w = min(kGroup, ncols - norm_next * kGroup) / 8;
+          norm_vectors<XS>(sm, norm_next * (kGroup / 8), w, p.M * w, tid, nthr);
+        }
+        ++norm_next;
+        norm_at = norm_next <= ngroups ? (norm_next - 1) * kGroup : -1;
       }
-      if (!mbar_wait(sm.xbar, xphase)) ok = false;
-      xphase ^= 1u;
-      if (NORM) {
-        for (int c8 = tid; c8 * 8 < nc; c8 += nthr) {
-          int k = c0 + t0 + c8 * 8;
-          if (k >= p.Kd) k -= p.Kd;
-          const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
-          for (int m = 0; m < p.M; ++m) {
-            uint4* ptr = reinterpret_cast<uint4*>(sm.xs + (size_t)m * XS + c8 * 8);
-            *ptr = norm8(*ptr, sm.s_rstd[m], gv);
+      int xcol = jw;
+      if (!one_chunk) {  // a window of several chunks, staged here chunk by chunk
+        const int xchunk = jw / XC;
+        xcol = jw - xchunk * XC;
+        if (xchunk != staged) {
+          const int t0 = xchunk * XC, nc = min(XC, ncols - t0);
+          fence_proxy_async_smem();  // earlier reads and writes of xs precede the bulk copies
+          named_sync(1, nthr);
+          if (tid == 0) stage_issue(p, sm.xs, XS, c0, t0, nc, sm.xbar);
+          if (NORM && staged < 0) {  // row rstd, one warp per row, while the copies fly
+            for (int m = warp; m < p.M; m += kLinConsumerWarps) {
+              float ss = 0.0f;
+              for (int t = lane; t < p.ss_tiles; t += 32) ss = __fadd_rn(ss, __ldcg(p.x_ss + m * p.ss_tiles + t));
+              for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+              if (lane == 0) sm.s_rstd[m] = 1.0f / sqrtf(ss / (float)p.Kd + p.eps);
+            }
+            named_sync(1, nthr);
+          }
+          if (!mbar_wait(sm.xbar, xphase)) ok = false;
+          xphase ^= 1u;
+          if (NORM) {
+            for (int c8 = tid; c8 * 8 < nc; c8 += nthr) {
+              int k = c0 + t0 + c8 * 8;
+              if (k >= Kd) k -= Kd;
+              const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
+              for (int m = 0; m < p.M; ++m) {
+                uint4* ptr = reinterpret_cast<uint4*>(sm.xs + (size_t)m * XS + c8 * 8);
+                *ptr = norm8(*ptr, sm.s_rstd[m], gv);
+              }
+            }
+          }
+          named_sync(1, nthr);
+          staged = xchunk;
+        }
+      }
+      const int s = it & (kLinStages - 1);
+      if (ok && !mbar_wait(&sm.full[s], (uint32_t)(it / kLinStages) & 1u)) ok = false;
+      if (ok) {
+        const uint32_t tile_base = smem_u32(sm.ring + s * kLinStageBytes + chunk * kLinChunkBytes);
+#pragma unroll
+        for (int k16 = 0; k16 < kLinBK / 16; ++k16) {
+          uint32_t a[4];
+          const int kc = k16 * 2 + a_khalf;
+          ldsm_x4(tile_base + a_row * 128 + ((kc ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            uint32_t b0, b1;
+            ldsm_x2(xs_base + (uint32_t)(((t * 8) * XS + xcol + k16 * 16) * sizeof(bf16)), b0, b1);
+            mma_bf16(acc[t], a, b0, b1);
           }
         }
       }
-      named_sync(1, nthr);
-      staged = xchunk;
+      fence_proxy_async_smem();  // our ldmatrix reads of stage s precede its next TMA write
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[s]);
+      jw += kLinBK;
+      if (jw == Kd) jw = 0;
     }
-    const int s = it % kLinStages;
-    if (ok && !mbar_wait(&sm.full[s], (it / kLinStages) & 1)) ok = false;
-    if (ok) {
-      const uint32_t tile_base = smem_u32(sm.ring + s * kLinStageBytes + chunk * kLinChunkBytes);
-      const uint32_t xcol = (uint32_t)(jw - xchunk * XC);
-#pragma unroll
-      for (int k16 = 0; k16 < kLinBK / 16; ++k16) {
-        uint32_t a[4];
-        const int kc = k16 * 2 + a_khalf;
-        ldsm_x4(tile_base + a_row * 128 + ((kc ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          uint32_t b0, b1;
-          ldsm_x2(xs_base + (uint32_t)(((t * 8) * XS + xcol + k16 * 16) * sizeof(bf16)), b0, b1);
-          mma_bf16(acc[t], a, b0, b1);
-        }
-      }
-    }
-    fence_proxy_async_smem();  // our ldmatrix reads of stage s precede its next TMA write
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[s]);
-
-    if (kk != KB - 1 && kb != kb_end - 1) continue;
-    // ------------ this CTA's part of `tile` is complete
-    epi_preload<MP, EPI>(p, tile, pos, cap, pre);
-    const int kk_first = kk - (int)(kb - seg_begin);
-    seg_begin = kb + 1;
+    // ------------ this CTA's part of the tile is complete (k-blocks kk_first..kk)
+    const int kk = kk0 + nblk - 1, kk_first = kk0, tile_done = tile;
+    left -= nblk;
+    ++tile;
+    kk0 = 0;
+    epi_preload<MP, EPI>(p, tile_done, pos, cap, pre);
     named_sync(1, nthr);  // the previous tile's epilogue is done with T
     if (kk_first == 0 && kk == KB - 1) {
 #pragma unroll
@@ -602,10 +607,10 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
         T[(lr0 + 8) * TS + m0 + 1] = acc[t][3];
       }
     } else {
-      const int c_first = owner_cta((long long)tile * KB, Tk, G);
-      const int c_last = owner_cta((long long)tile * KB + KB - 1, Tk, G);
+      const int c_first = owner_cta((long long)tile_done * KB, Tk, G);
+      const int c_last = owner_cta((long long)tile_done * KB + KB - 1, Tk, G);
       const int nseg = c_last - c_first + 1, seg = cta - c_first;
-      float* wsb = p.ws + ((size_t)(tile * p.max_seg + seg) * kLinRows) * MP;
+      float* wsb = p.ws + ((size_t)(tile_done * p.max_seg + seg) * kLinRows) * MP;
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const int m0 = t * 8 + 2 * q;
@@ -620,7 +625,7 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
         unsigned prev;
         asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
                      : "=r"(prev)
-                     : "l"(reinterpret_cast<unsigned*>(p.counters + tile))
+                     : "l"(reinterpret_cast<unsigned*>(p.counters + tile_done))
                      : "memory");
         *sm.s_flag = (prev == (unsigned)(nseg - 1));
       }
@@ -628,7 +633,7 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
       const bool last = *sm.s_flag != 0;
       if (last) {
         // last CTA of this tile: sum the partials of its CTAs in k order
-        const float* wst = p.ws + ((size_t)tile * p.max_seg * kLinRows) * MP;
+        const float* wst = p.ws + ((size_t)tile_done * p.max_seg * kLinRows) * MP;
         for (int e = tid; e < kLinRows * p.M; e += nthr) {
           const int lr = e / p.M, m = e % p.M;
           float part[kLinMaxSeg];
@@ -641,7 +646,7 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
             if (j < nseg) v = __fadd_rn(v, part[j]);
           T[lr * TS + m] = v;
         }
-        if (tid == 0) p.counters[tile] = 0;  // ready for the next use
+        if (tid == 0) p.counters[tile_done] = 0;  // ready for the next use
       }
 #pragma unroll
       for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
@@ -651,13 +656,13 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
     for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
     named_sync(1, nthr);
     if (EPI == EPI_QKV)
-      epilogue_qkv<MP>(p, tile, T, TS, sm.s_hrstd, pos, pre);
+      epilogue_qkv<MP>(p, tile_done, T, TS, sm.s_hrstd, pos, pre);
     else if (EPI == EPI_RESID)
-      epilogue_resid<MP>(p, tile, T, TS, pre);
+      epilogue_resid<MP>(p, tile_done, T, TS, pre);
     else if (EPI == EPI_GLU)
-      epilogue_glu(p, tile, T, TS);
+      epilogue_glu(p, tile_done, T, TS);
     else
-      epilogue_logits(p, tile, T, TS);
+      epilogue_logits(p, tile_done, T, TS);
   }
   return ok;
 }

@@ -28,7 +28,7 @@ struct sv_ctx {
   cudaEvent_t ev = nullptr;
   bool use_graphs = true;
   bool use_pdl = true;  // chain a step's kernels with programmatic dependent launch
-  bool use_prefetch = false;  // each linear prefetches the start of the next one into L2
+  int prefetch_mode = 0;  // 0 none, 1 every linear prefetches the next one into L2, 2 only QKV -> O
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
   std::vector<const bf16*> attn_norm, q_norm, k_norm, ffn_norm;
@@ -264,7 +264,8 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   // last one's next is the first of the following step)
   const bool head = mode != MODE_BODY;
   auto next_of = [&](int which, int l) -> const LinearDesc* {
-    if (!ctx->use_prefetch) return nullptr;
+    if (ctx->prefetch_mode == 0) return nullptr;
+    if (ctx->prefetch_mode == 2) return which == LIN_QKV ? &ctx->lin_o[l] : nullptr;
     switch (which) {
       case LIN_QKV: return &ctx->lin_o[l];
       case LIN_O: return &ctx->lin_gu[l];
@@ -451,7 +452,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   // Off by default: on the 8B-shaped verify step it measured 2 % slower (the
   // prefetches compete with the slowest CTAs of the current launch).
   const char* pf = getenv("SV_L2_PREFETCH");
-  ctx->use_prefetch = pf && pf[0] == '1';
+  ctx->prefetch_mode = pf ? atoi(pf) : 0;
   if (prepare_linear_kernels() != cudaSuccess || prepare_attention_kernels() != cudaSuccess)
     return bail(SV_E_CUDA);
 
@@ -749,7 +750,7 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
       p.grid = ld->grid;
       // the same class of the next layer is prefetched, as much as inside a step
       const LinearDesc* next = nullptr;
-      if (ctx->use_prefetch && which != SV_LIN_LM_HEAD) {
+      if (ctx->prefetch_mode == 1 && which != SV_LIN_LM_HEAD) {
         const int ln = (l + 1) % c.n_layers;
         next = which == SV_LIN_O ? &ctx->lin_o[ln]
                                  : (which == SV_LIN_GATE_UP ? &ctx->lin_gu[ln] : &ctx->lin_down[ln]);
