@@ -3,8 +3,9 @@
 // Row r of a step attends to positions [0, pos + r + 1) ("Phase 23:
 // Speculative Verify Parity" section 2 step 2: one metadata row per draft
 // token with context length pos+1 upward).  Work is split over absolute
-// positions: split s covers [256 s, 256 s + 256) and warp w of the CTA covers
-// [256 s + 64 w, +64), four 16-position pages.  Because these boundaries are
+// positions: split s covers [256 s, 256 s + 256) and warp w of the CTA a fixed
+// run of its 16-position pages (two pages per warp for head_dim <= 128, four
+// for 256).  Because these boundaries are
 // absolute, the partial result a row gets from a split does not depend on how
 // many other rows share the step, on the cache's history, or on its physical
 // pages; positions a row may not see are masked to exact zeros.  Partials are
@@ -28,16 +29,20 @@ namespace {
 
 template <int D>
 struct AttnCfg {
+  // warps per CTA, each over kPagesPerWarp consecutive 16-position pages of the split
+  static constexpr int kWarps = D <= 128 ? 8 : 4;
+  static constexpr int kPagesPerWarp = kAttnSplit / kPage / kWarps;
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kBoxes = D / 64;                // 64-column boxes per page row
   static constexpr int kPageBytes = kPage * D * 2;     // one K (or V) page of one head
   static constexpr int kBufBytes = 2 * kPageBytes;     // K + V
-  static constexpr int kBufs = D <= 128 ? 4 : 2;       // pages in flight per warp
+  static constexpr int kBufs = kPagesPerWarp < 2 ? kPagesPerWarp : 2;  // pages in flight per warp
   static constexpr int kQStride = D + 8;               // bf16 elements
-  static constexpr int kRingBytes = kAttnWarps * kBufs * kBufBytes;
+  static constexpr int kRingBytes = kWarps * kBufs * kBufBytes;
   static constexpr int kQBytes = 16 * kQStride * 2;
-  static constexpr int kScratchBytes = kAttnWarps * 16 * (D + 2) * 4;
+  static constexpr int kScratchBytes = kWarps * 16 * (D + 2) * 4;
   static constexpr int kSmem = 1024 + (kRingBytes > kScratchBytes ? kRingBytes : kScratchBytes) +
-                               kQBytes + kAttnWarps * kBufs * 8 + 64;
+                               kQBytes + kWarps * kBufs * 8 + 64;
 };
 
 // Shared memory of the attention work: per-warp page buffers (aliased by the
@@ -59,19 +64,19 @@ struct AttnSmem {
   static constexpr int bytes() {
     using C = AttnCfg<D>;
     return (C::kRingBytes > C::kScratchBytes ? C::kRingBytes : C::kScratchBytes) + C::kQBytes +
-           kAttnWarps * C::kBufs * 8;
+           C::kWarps * C::kBufs * 8;
   }
 };
 
 // Initialise the page barriers (one thread).
 template <int D>
 __device__ __forceinline__ void attn_init_bars(const AttnSmem<D>& sm) {
-  for (int i = 0; i < kAttnWarps * AttnCfg<D>::kBufs; ++i) mbar_init(&sm.bars[i], 1);
+  for (int i = 0; i < AttnCfg<D>::kWarps * AttnCfg<D>::kBufs; ++i) mbar_init(&sm.bars[i], 1);
   fence_barrier_init();
 }
 
 // Work items w = cta, cta + G_ctas, ... of this step's attention, run by
-// warps 0..kAttnWarps-1 (named barrier 2).  `phase` holds each buffer's
+// the CTA's AttnCfg<D>::kWarps warps (named barrier 2).  `phase` holds each buffer's
 // parity.  `pos` is the committed length, final for the whole step: the
 // pages of the first item that hold only positions < pos (written by earlier
 // steps) are requested before the wait on the previous kernel; Q and the page
@@ -116,11 +121,11 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
     const int ctx_max = pos + r0 + nrows;  // largest context of the block's rows
 
     // ---- this warp's four pages
-    const int wpos0 = split * kAttnSplit + warp * (kAttnPagesPerWarp * kPage);
+    const int wpos0 = split * kAttnSplit + warp * (C::kPagesPerWarp * kPage);
     int npages = 0;
-    while (npages < kAttnPagesPerWarp && wpos0 + npages * kPage < ctx_max) ++npages;
-    int page_id[kAttnPagesPerWarp];
-    for (int j = 0; j < kAttnPagesPerWarp; ++j) {
+    while (npages < C::kPagesPerWarp && wpos0 + npages * kPage < ctx_max) ++npages;
+    int page_id[C::kPagesPerWarp];
+    for (int j = 0; j < C::kPagesPerWarp; ++j) {
       int pg = -1;
       if (j < npages) {
         const int lp = (wpos0 + j * kPage) / kPage;
@@ -160,7 +165,7 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       for (int j = n_old; j < npages && j < C::kBufs; ++j) issue(j);
     }
     // ---- Q tile: query qi = (token row r0 + qi / G, head h G + qi % G)
-    for (int v = tid; v < 16 * (D / 8); v += kAttnWarps * 32) {
+    for (int v = tid; v < 16 * (D / 8); v += C::kThreads) {
       const int qi = v / (D / 8), c8 = v % (D / 8);
       uint4 val = make_uint4(0u, 0u, 0u, 0u);
       if (qi < nrows * G) {
@@ -169,7 +174,7 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       }
       *reinterpret_cast<uint4*>(Qs + qi * C::kQStride + c8 * 8) = val;
     }
-    named_sync(2, kAttnWarps * 32);
+    named_sync(2, C::kThreads);
 
     // query rows held by this lane: g and g + 8
     const int ctx_lo = pos + r0 + g / G + 1;
@@ -265,7 +270,7 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       if (lane == 0 && j + C::kBufs < npages) issue(j + C::kBufs);
     }
     if (!ok) all_ok = false;
-    named_sync(2, kAttnWarps * 32);  // every warp is done with its ring: reuse it as scratch
+    named_sync(2, C::kThreads);  // every warp is done with its ring: reuse it as scratch
 
     // ---- per-warp partials to scratch: [warp][16][D + 2] (m, l, o[D])
     float* sw = scratch + warp * 16 * (D + 2);
@@ -283,14 +288,14 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       sw[(g + 8) * (D + 2) + 2 + c] = o[n][2];
       sw[(g + 8) * (D + 2) + 3 + c] = o[n][3];
     }
-    named_sync(2, kAttnWarps * 32);
+    named_sync(2, C::kThreads);
     // ---- merge the warps in order 0..3 and write the split partial
     const int nq = nrows * G;
-    for (int e = tid; e < nq * (D / 8); e += kAttnWarps * 32) {
+    for (int e = tid; e < nq * (D / 8); e += C::kThreads) {
       const int qi = e / (D / 8), c0 = (e % (D / 8)) * 8;
-      float mw[kAttnWarps], mx = -INFINITY;
+      float mw[C::kWarps], mx = -INFINITY;
 #pragma unroll
-      for (int ww = 0; ww < kAttnWarps; ++ww) {
+      for (int ww = 0; ww < C::kWarps; ++ww) {
         mw[ww] = scratch[(ww * 16 + qi) * (D + 2)];
         mx = fmaxf(mx, mw[ww]);
       }
@@ -299,7 +304,7 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
       if (mx != -INFINITY) {
 #pragma unroll
-        for (int ww = 0; ww < kAttnWarps; ++ww) {
+        for (int ww = 0; ww < C::kWarps; ++ww) {
           if (mw[ww] == -INFINITY) continue;
           const float sc = exp2f(__fsub_rn(mw[ww], mx));
           const float* src = scratch + (ww * 16 + qi) * (D + 2);
@@ -316,7 +321,7 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
     fence_proxy_async_smem();  // scratch (in the ring) is overwritten by TMA next item
-    named_sync(2, kAttnWarps * 32);            // scratch (= ring) and Qs are rewritten by the next item
+    named_sync(2, C::kThreads);            // scratch (= ring) and Qs are rewritten by the next item
   }
   return all_ok;
 }

@@ -3,8 +3,9 @@
 // Row r of a step attends to positions [0, pos + r + 1) ("Phase 23:
 // Speculative Verify Parity" section 2 step 2: one metadata row per draft
 // token with context length pos+1 upward).  Work is split over absolute
-// positions: split s covers [256 s, 256 s + 256) and warp w of the CTA covers
-// [256 s + 64 w, +64), four 16-position pages.  Because these boundaries are
+// positions: split s covers [256 s, 256 s + 256) and warp w of the CTA a fixed
+// run of its 16-position pages (two pages per warp for head_dim <= 128, four
+// for 256).  Because these boundaries are
 // absolute, the partial result a row gets from a split does not depend on how
 // many other rows share the step, on the cache's history, or on its physical
 // pages; positions a row may not see are masked to exact zeros.  Partials are
@@ -26,7 +27,7 @@ namespace sv {
 namespace {
 
 template <int D>
-__global__ void __launch_bounds__(kAttnWarps * 32, 1)
+__global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -62,7 +63,7 @@ cudaError_t launch_attn_t(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   auto kern = k_attention<D>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kAttnWarps * 32);
+  cfg.blockDim = dim3(AttnCfg<D>::kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

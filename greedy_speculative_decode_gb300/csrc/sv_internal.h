@@ -37,9 +37,7 @@ constexpr int kLinConsumerWarps = 8;
 constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;  // consumers, then the TMA producer
 
 // Attention geometry: a split is 256 absolute positions = 4 warps x 4 pages.
-constexpr int kAttnWarps = 4;
-constexpr int kAttnPagesPerWarp = 4;
-constexpr int kAttnSplit = kAttnWarps * kAttnPagesPerWarp * kPage;  // 256
+constexpr int kAttnSplit = 256;  // positions per split (split s: [256 s, 256 s + 256))
 constexpr int kAttnQ = 16;  // query rows (token rows x heads of one group) per work item
 
 // Kinds of linear epilogue.
