@@ -219,9 +219,13 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
           const int ctx = e < 2 ? ctx_lo : ctx_hi;
           s[nt][e] = pabs < ctx ? __fmul_rn(s[nt][e], p.scale_log2) : -INFINITY;
         }
-      // online softmax on rows g (e = 0, 1) and g + 8 (e = 2, 3)
+      // online softmax on rows g (e = 0, 1) and g + 8 (e = 2, 3).  The weights
+      // p stay fp32: the denominator sums them unrounded, and P V is taken as
+      // P_hi V + P_lo V with P_hi = bf16(p) and P_lo = bf16(p - P_hi) (the
+      // tensor cores take bf16), which carries p to about 2^-16 -- a bf16-only
+      // P would shift every attention output by up to half a bf16 step.
       float alpha[2];
-      uint32_t pa[4];
+      uint32_t pa[4], pl[4];
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
         float mx = fmaxf(fmaxf(s[0][2 * rr], s[0][2 * rr + 1]), fmaxf(s[1][2 * rr], s[1][2 * rr + 1]));
@@ -234,10 +238,10 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
           pv[0] = pv[1] = pv[2] = pv[3] = 0.0f;
         } else {
           alpha[rr] = exp2f(__fsub_rn(m_run[rr], m_new));
-          pv[0] = bf16r(exp2f(__fsub_rn(s[0][2 * rr], m_new)));
-          pv[1] = bf16r(exp2f(__fsub_rn(s[0][2 * rr + 1], m_new)));
-          pv[2] = bf16r(exp2f(__fsub_rn(s[1][2 * rr], m_new)));
-          pv[3] = bf16r(exp2f(__fsub_rn(s[1][2 * rr + 1], m_new)));
+          pv[0] = exp2f(__fsub_rn(s[0][2 * rr], m_new));
+          pv[1] = exp2f(__fsub_rn(s[0][2 * rr + 1], m_new));
+          pv[2] = exp2f(__fsub_rn(s[1][2 * rr], m_new));
+          pv[3] = exp2f(__fsub_rn(s[1][2 * rr + 1], m_new));
         }
         float sum = __fadd_rn(__fadd_rn(pv[0], pv[1]), __fadd_rn(pv[2], pv[3]));
         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, 1));
@@ -246,6 +250,8 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
         m_run[rr] = m_new;
         pa[rr] = pack_bf16x2(pv[0], pv[1]);      // positions 2q, 2q+1
         pa[2 + rr] = pack_bf16x2(pv[2], pv[3]);  // positions 8+2q, 9+2q
+        pl[rr] = pack_bf16x2(__fsub_rn(pv[0], bf16r(pv[0])), __fsub_rn(pv[1], bf16r(pv[1])));
+        pl[2 + rr] = pack_bf16x2(__fsub_rn(pv[2], bf16r(pv[2])), __fsub_rn(pv[3], bf16r(pv[3])));
       }
 #pragma unroll
       for (int n = 0; n < D / 8; ++n) {
@@ -254,8 +260,9 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
         o[n][2] = __fmul_rn(o[n][2], alpha[1]);
         o[n][3] = __fmul_rn(o[n][3], alpha[1]);
       }
-      // O += P V
+      // O += P_hi V + P_lo V
       const uint32_t afr[4] = {pa[0], pa[1], pa[2], pa[3]};
+      const uint32_t afl[4] = {pl[0], pl[1], pl[2], pl[3]};
 #pragma unroll
       for (int dn = 0; dn < D / 16; ++dn) {
         const int pr = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -264,6 +271,8 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
         ldsm_x4_trans(vb + ((dn * 16) >> 6) * 2048 + pr * 128 + ((ch ^ (pr & 7)) << 4), b0, b1, b2, b3);
         mma_bf16(o[2 * dn], afr, b0, b1);
         mma_bf16(o[2 * dn + 1], afr, b2, b3);
+        mma_bf16(o[2 * dn], afl, b0, b1);
+        mma_bf16(o[2 * dn + 1], afl, b2, b3);
       }
       fence_proxy_async_smem();  // reads of buffer b precede its next TMA write
       __syncwarp();

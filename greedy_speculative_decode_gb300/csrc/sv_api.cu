@@ -52,7 +52,8 @@ struct sv_ctx {
   float* am_val = nullptr;
   int* am_idx = nullptr;
   // pinned host staging
-  int32_t* pin_in = nullptr;   // [cap_len, tokens...] per row block, max_seq + kMaxK + 1 slots
+  int32_t* pin_in = nullptr;   // [cap_len, tokens...] per row block of one call
+  size_t pin_in_len = 0;       // ints: max_seq + one cap_len slot per block of a full prefill
   int32_t* pin_out = nullptr;  // result[4] + seq_len + status
   int* pin_bt = nullptr;       // block table mirror
   // host-side sequence state
@@ -376,6 +377,8 @@ int end_call(sv_ctx* ctx) {
 // Stage [cap_len, tokens[0..n)] at slot `at` of the pinned input buffer and
 // copy it into the device state.
 int upload_tokens(sv_ctx* ctx, const int32_t* tokens, int n, int at) {
+  if (at < 0 || (size_t)at + n + 1 > ctx->pin_in_len)
+    return fail(ctx, SV_E_INVAL, "token staging of %d at %d exceeds %zu", n, at, ctx->pin_in_len);
   int32_t* src = ctx->pin_in + at;
   src[0] = ctx->n_alloc * kPage;
   memcpy(src + 1, tokens, n * sizeof(int32_t));
@@ -524,7 +527,9 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   if (!make_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
       !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage))
     return bail(SV_E_CUDA);
-  if (cudaMallocHost(&ctx->pin_in, sizeof(int32_t) * ((size_t)c.max_seq + 2 * kMaxK + 8)) != cudaSuccess ||
+  // a prefill of max_seq tokens stages every block [cap_len, tokens] side by side
+  ctx->pin_in_len = (size_t)c.max_seq + (c.max_seq + c.max_k - 1) / c.max_k + kMaxK + 8;
+  if (cudaMallocHost(&ctx->pin_in, sizeof(int32_t) * ctx->pin_in_len) != cudaSuccess ||
       cudaMallocHost(&ctx->pin_out, sizeof(int32_t) * 8) != cudaSuccess ||
       cudaMallocHost(&ctx->pin_bt, sizeof(int) * (size_t)ctx->bt_len) != cudaSuccess)
     return bail(SV_E_NOMEM);

@@ -48,6 +48,15 @@ def assert_close_to_oracle(gpu_logits, orc_logits, what=""):
     return err
 
 
+def decisive(orc_logits, rows) -> bool:
+    """True if the oracle's top-2 margin exceeds ARGMAX_MARGIN on every row in
+    ``rows``: only then is its greedy choice, and so its acceptance count, one
+    the GPU must reproduce (closer calls are bf16 near-ties)."""
+    o = np.atleast_2d(np.asarray(orc_logits, dtype=np.float64))
+    top2 = np.sort(o[list(rows)], axis=1)[:, -2:]
+    return bool(np.all(top2[:, 1] - top2[:, 0] > ARGMAX_MARGIN))
+
+
 def bits(t):
     """Raw bytes of a CUDA tensor as a numpy uint8 array (for exact comparisons)."""
     import torch
