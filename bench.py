@@ -193,7 +193,7 @@ def step_bytes(cfg, K, pos):
 
 def kernel_hash():
     h = hashlib.sha256()
-    for f in ("k_linear.cu", "sv_ptx.cuh", "sv_internal.h"):
+    for f in ("k_linear.cu", "lin_dev.cuh", "sv_ptx.cuh", "sv_internal.h"):
         with open(os.path.join(ROOT, "greedy_speculative_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -202,7 +202,7 @@ def kernel_hash():
 def ncu_traffic():
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "traffic_k_linear_gate_up_qwen3_8b.txt")
     try:
         with open(path) as f:
             t = json.load(f)
