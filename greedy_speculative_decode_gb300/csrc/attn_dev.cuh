@@ -336,21 +336,41 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
 }
 
 // One element of the split merge: out[r, hq, i] from the split partials s <
-// ceil((pos + r + 1) / 256), merged in order.
+// ceil((pos + r + 1) / 256), merged in order.  The partials of up to eight
+// splits (contexts up to 2048) are requested together; longer contexts take
+// the maximum in a first pass and accumulate in a second, eight at a time.
 template <int D>
 __device__ __forceinline__ void combine_element(const AttnParams& p, int r, int hq, int i, int pos) {
+  constexpr int kChunk = 8;
   const int ctx = pos + r + 1;
   const int ns = (ctx + kAttnSplit - 1) / kAttnSplit;
   const size_t base = ((size_t)r * p.n_q_heads + hq) * p.max_splits;
+  float2 ml[kChunk];
+  float ov[kChunk];
   float mx = -INFINITY;
-  for (int s = 0; s < ns; ++s) mx = fmaxf(mx, __ldcg(&p.part_ml[base + s].x));
+  if (ns > kChunk)
+    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, __ldcg(&p.part_ml[base + s].x));
   float L = 0.0f, acc = 0.0f;
-  for (int s = 0; s < ns; ++s) {
-    const float2 ml = __ldcg(&p.part_ml[base + s]);
-    if (ml.x == -INFINITY) continue;
-    const float sc = exp2f(__fsub_rn(ml.x, mx));
-    L = __fadd_rn(L, __fmul_rn(ml.y, sc));
-    acc = __fadd_rn(acc, __fmul_rn(__ldcg(&p.part_o[(base + s) * D + i]), sc));
+  for (int s0 = 0; s0 < ns; s0 += kChunk) {
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      if (s0 + j < ns) {
+        ml[j] = __ldcg(&p.part_ml[base + s0 + j]);
+        ov[j] = __ldcg(&p.part_o[(base + s0 + j) * D + i]);
+      }
+    }
+    if (ns <= kChunk) {
+#pragma unroll
+      for (int j = 0; j < kChunk; ++j)
+        if (j < ns) mx = fmaxf(mx, ml[j].x);
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      if (s0 + j >= ns || ml[j].x == -INFINITY) continue;
+      const float sc = exp2f(__fsub_rn(ml[j].x, mx));
+      L = __fadd_rn(L, __fmul_rn(ml[j].y, sc));
+      acc = __fadd_rn(acc, __fmul_rn(ov[j], sc));
+    }
   }
   p.out[(size_t)r * p.n_q_heads * D + hq * D + i] = __float2bfloat16_rn(__fdiv_rn(acc, L));
   asm volatile("fence.proxy.async.global;" ::: "memory");  // read next by bulk copies
