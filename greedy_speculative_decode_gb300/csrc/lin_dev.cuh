@@ -95,6 +95,23 @@ __device__ __forceinline__ void epi_preload(const LinParams& p, int tile, int po
       if (e < kLinRows * p.M)
         pre.res[j] = ldcg_bf16(p.out + (size_t)(e / kLinRows) * p.out_stride + tile * kLinRows + e % kLinRows);
     }
+  } else if (EPI == EPI_QKV && p.head_dim == kLinRows) {
+    // one head per tile, one warp per token row (see epilogue_qkv): row
+    // m = warp + 8 k, lane's RoPE angles for elements lane and lane + 32
+    const int warp = tid >> 5, lane = tid & 31, half = kLinRows / 2;
+    const bool kv = tile * kLinRows >= p.n_q_heads * kLinRows;
+#pragma unroll
+    for (int k = 0; k < MP / 8; ++k) {
+      const int m = warp + 8 * k;
+      pre.cs[2 * k] = pre.cs[2 * k + 1] = make_float2(1.0f, 0.0f);
+      pre.page[k] = -1;
+      if (m < p.M) {
+        const float2* rp = p.rope + (size_t)(pos + m) * half;
+        pre.cs[2 * k] = rp[lane];
+        pre.cs[2 * k + 1] = rp[lane + 32];
+        if (kv && pos + m < cap) pre.page[k] = p.block_table[(pos + m) / kPage];
+      }
+    }
   } else if (EPI == EPI_QKV) {
     const TileRows tr = tile_rows(p, tile);
     const int d = p.head_dim, half = d / 2;
@@ -122,8 +139,64 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
                              const EpiPre<MP>& pre) {
   const int tid = threadIdx.x, M = p.M, d = p.head_dim;
   const int nthr = kLinConsumerWarps * 32;
-  const TileRows tr = tile_rows(p, tile);
   const int qrows = p.n_q_heads * d, krows = p.n_kv_heads * d;
+  if (d == kLinRows) {
+    // The tile is exactly one head (q, k or v).  One warp per token row; lane
+    // holds elements i = lane + 32 j, j = 0..3, so the head's norm is a warp
+    // reduction and the RoPE partners (i, i + 64) sit in the same lane: no
+    // CTA barrier.  Same arithmetic, in the same order, as the general path.
+    const int warp = tid >> 5, lane = tid & 31;
+    const int f0 = tile * kLinRows, head = tile;
+    const bool is_q = f0 < qrows, is_k = !is_q && f0 < qrows + krows;
+#pragma unroll
+    for (int k = 0; k < MP / 8; ++k) {
+      const int m = warp + 8 * k;
+      if (m >= M) break;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = bf16r(T[(lane + 32 * j) * TS + m]);
+      if (p.q_gain != nullptr && (is_q || is_k)) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ss = __fadd_rn(ss, __fmul_rn(v[j], v[j]));
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        const float r = 1.0f / sqrtf(ss / (float)d + p.eps);
+        const bf16* g = is_q ? p.q_gain : p.k_gain;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[j] = bf16r(__fmul_rn(bf16r(__fmul_rn(v[j], r)), __bfloat162float(g[lane + 32 * j])));
+      }
+      float outv[4] = {v[0], v[1], v[2], v[3]};
+      if (is_q || is_k) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // pairs (j, j + 2): elements i and i + 64
+          const float2 cs = pre.cs[2 * k + h];
+          outv[h] = __fsub_rn(__fmul_rn(v[h], cs.x), __fmul_rn(v[h + 2], cs.y));
+          outv[h + 2] = __fadd_rn(__fmul_rn(v[h + 2], cs.x), __fmul_rn(v[h], cs.y));
+        }
+      }
+      if (is_q) {
+        bf16* dst = p.out + (size_t)m * p.out_stride + f0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = __float2bfloat16_rn(outv[j]);
+      } else {
+        const int page = pre.page[k], ps = pos + m;
+        if (page < 0) {
+          if (lane == 0) atomicOr(&p.st->status, ST_BAD_PAGE);
+          continue;
+        }
+        const int kvh = is_k ? head - p.n_q_heads : head - p.n_q_heads - p.n_kv_heads;
+        bf16* dst = (is_k ? p.kcache : p.vcache) +
+                    (((size_t)page * p.n_kv_heads + kvh) * kPage + (ps % kPage)) * d;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = __float2bfloat16_rn(outv[j]);
+      }
+    }
+    // the cached K/V are read next through TMA (the async proxy)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return;
+  }
+  const TileRows tr = tile_rows(p, tile);
   // 1. round the projection to bf16
   for (int e = tid; e < kLinRows * M; e += nthr) {
     int lr = e % kLinRows, m = e / kLinRows;
