@@ -74,8 +74,10 @@ __device__ __forceinline__ float act_fn(float g, int act) {
 // Epilogue operands that live in global memory, loaded for a tile as soon as
 // the CTA has finished its share of it -- before it learns whether it is the
 // CTA that completes the tile -- so their latency overlaps the exchange of
-// partial sums.  Element j of thread tid is e = tid + j * 256: row lr = e mod
-// 128 of the tile, token row m = e / 128 (the epilogues' own order).
+// partial sums.  Each is held by the thread whose epilogue uses it: in the
+// one-warp-per-token-row epilogues, warp w takes rows m = w + 8 k and lane l
+// the tile rows l + 32 j; in the general QKV epilogue, element j of thread tid
+// is e = tid + j * 256 (tile row e mod 128, token row e / 128).
 template <int MP>
 struct EpiPre {
   static constexpr int N = (kLinRows * MP + kLinConsumerWarps * 32 - 1) / (kLinConsumerWarps * 32);
@@ -88,12 +90,16 @@ template <int MP, int EPI>
 __device__ __forceinline__ void epi_preload(const LinParams& p, int tile, int pos, int cap,
                                             EpiPre<MP>& pre) {
   const int tid = threadIdx.x, nthr = kLinConsumerWarps * 32;
-  if (EPI == EPI_RESID) {
+  if (EPI == EPI_RESID) {  // warp w: rows m = w + 8 k, elements lane + 32 j (see epilogue_resid)
+    const int warp = tid >> 5, lane = tid & 31;
 #pragma unroll
-    for (int j = 0; j < EpiPre<MP>::N; ++j) {
-      const int e = tid + j * nthr;
-      if (e < kLinRows * p.M)
-        pre.res[j] = ldcg_bf16(p.out + (size_t)(e / kLinRows) * p.out_stride + tile * kLinRows + e % kLinRows);
+    for (int k = 0; k < MP / 8; ++k) {
+      const int m = warp + 8 * k;
+      if (m < p.M) {
+        const bf16* row = p.out + (size_t)m * p.out_stride + tile * kLinRows + lane;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pre.res[4 * k + j] = ldcg_bf16(row + 32 * j);
+      }
     }
   } else if (EPI == EPI_QKV && p.head_dim == kLinRows) {
     // one head per tile, one warp per token row (see epilogue_qkv): row
@@ -270,26 +276,23 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Residual epilogue: x[m, n0 + lr] += bf16(T[lr, m]) (rounded to bf16), and
+// the tile's sum of squares of each new row for the next RMSNorm.  One warp
+// per token row, lane l holding tile rows l + 32 j: no CTA barrier.
 template <int MP>
 __device__ void epilogue_resid(const LinParams& p, int tile, float* T, int TS, const EpiPre<MP>& pre) {
-  const int tid = threadIdx.x, M = p.M, nthr = kLinConsumerWarps * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = tile * kLinRows;
 #pragma unroll
-  for (int j = 0; j < EpiPre<MP>::N; ++j) {
-    const int e = tid + j * nthr;
-    if (e >= kLinRows * M) break;
-    int lr = e % kLinRows, m = e / kLinRows;
-    size_t o = (size_t)m * p.out_stride + n0 + lr;
-    float v = bf16r(__fadd_rn(pre.res[j], bf16r(T[lr * TS + m])));
-    p.out[o] = __float2bfloat16_rn(v);
-    T[lr * TS + m] = v;
-  }
-  named_sync(1, nthr);
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int m = warp; m < M; m += kLinConsumerWarps) {
+  for (int k = 0; k < MP / 8; ++k) {
+    const int m = warp + 8 * k;
+    if (m >= p.M) break;
+    bf16* row = p.out + (size_t)m * p.out_stride + n0 + lane;
     float ss = 0.0f;
-    for (int j = 0; j < kLinRows / 32; ++j) {
-      float v = T[(lane + 32 * j) * TS + m];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float v = bf16r(__fadd_rn(pre.res[4 * k + j], bf16r(T[(lane + 32 * j) * TS + m])));
+      row[32 * j] = __float2bfloat16_rn(v);
       ss = __fadd_rn(ss, __fmul_rn(v, v));
     }
     for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
@@ -311,35 +314,36 @@ __device__ void epilogue_glu(const LinParams& p, int tile, const float* T, int T
   asm volatile("fence.proxy.async.global;" ::: "memory");  // read next by bulk copies
 }
 
+// LM-head epilogue: bf16 logits (stored for rows m >= logits_row0 when a
+// buffer is given) and the tile's argmax of each row: largest value, lowest id
+// among equal values.  One warp per token row; lane l scans tile rows 4 l ..
+// 4 l + 3 in order, then a fixed xor tree combines the lanes.
+template <int MP>
 __device__ void epilogue_logits(const LinParams& p, int tile, float* T, int TS) {
-  const int tid = threadIdx.x, M = p.M, nthr = kLinConsumerWarps * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = tile * kLinRows;
-  for (int e = tid; e < kLinRows * M; e += nthr) {
-    int lr = e % kLinRows, m = e / kLinRows;
-    float v = bf16r(T[lr * TS + m]);
-    T[lr * TS + m] = v;
-    if (p.logits != nullptr && m >= p.logits_row0 && n0 + lr < p.vocab)
-      p.logits[(size_t)(m - p.logits_row0) * p.vocab + n0 + lr] = v;
-  }
-  named_sync(1, nthr);
-  const int warp = tid >> 5, lane = tid & 31;
-  for (int m = warp; m < M; m += kLinConsumerWarps) {
-    // each lane scans 4 consecutive rows in order, then a fixed tree picks the
-    // largest value, the lowest id among equal values
+#pragma unroll
+  for (int k = 0; k < MP / 8; ++k) {
+    const int m = warp + 8 * k;
+    if (m >= p.M) break;
+    const bool store = p.logits != nullptr && m >= p.logits_row0;
+    float* lrow = store ? p.logits + (size_t)(m - p.logits_row0) * p.vocab + n0 : nullptr;
     float best = -INFINITY;
     int bidx = 0x7fffffff;
+#pragma unroll
     for (int j = 0; j < 4; ++j) {
-      int lr = lane * 4 + j;
+      const int lr = lane * 4 + j;
       if (n0 + lr >= p.vocab) continue;
-      float v = T[lr * TS + m];
+      const float v = bf16r(T[lr * TS + m]);
+      if (store) lrow[lr] = v;
       if (bidx == 0x7fffffff || v > best) {
         best = v;
         bidx = n0 + lr;
       }
     }
     for (int o = 1; o < 32; o <<= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
       if (ov > best || (ov == best && oi < bidx)) {
         best = ov;
         bidx = oi;
@@ -735,7 +739,7 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
     else if (EPI == EPI_GLU)
       epilogue_glu(p, tile_done, T, TS);
     else
-      epilogue_logits(p, tile_done, T, TS);
+      epilogue_logits<MP>(p, tile_done, T, TS);
   }
   return ok;
 }
