@@ -40,7 +40,11 @@ struct AttnCfg {
   static constexpr int kQStride = D + 8;               // bf16 elements
   static constexpr int kRingBytes = kWarps * kBufs * kBufBytes;
   static constexpr int kQBytes = 16 * kQStride * 2;
-  static constexpr int kScratchBytes = kWarps * 16 * (D + 2) * 4;
+  // warp-merge scratch: o rows of stride kOS floats (kOS = 8 mod 32 banks, so a
+  // warp's float2 stores and float4 loads take the minimum two wavefronts),
+  // then the (m, l) pairs
+  static constexpr int kOS = D + 8;
+  static constexpr int kScratchBytes = kWarps * 16 * kOS * 4 + kWarps * 16 * 8;
   static constexpr int kSmem = 1024 + (kRingBytes > kScratchBytes ? kRingBytes : kScratchBytes) +
                                kQBytes + kWarps * kBufs * 8 + 64;
 };
@@ -281,32 +285,33 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
     if (!ok) all_ok = false;
     named_sync(2, C::kThreads);  // every warp is done with its ring: reuse it as scratch
 
-    // ---- per-warp partials to scratch: [warp][16][D + 2] (m, l, o[D])
-    float* sw = scratch + warp * 16 * (D + 2);
+    // ---- per-warp partials to scratch: o [warp][16][kOS], (m, l) [warp][16]
+    float* so = scratch;
+    float2* sml = reinterpret_cast<float2*>(scratch + C::kWarps * 16 * C::kOS);
     if (q4 == 0) {
-      sw[g * (D + 2)] = m_run[0];
-      sw[g * (D + 2) + 1] = l_run[0];
-      sw[(g + 8) * (D + 2)] = m_run[1];
-      sw[(g + 8) * (D + 2) + 1] = l_run[1];
+      sml[warp * 16 + g] = make_float2(m_run[0], l_run[0]);
+      sml[warp * 16 + g + 8] = make_float2(m_run[1], l_run[1]);
     }
+    {
+      float* r0p = so + (warp * 16 + g) * C::kOS + 2 * q4;
+      float* r1p = r0p + 8 * C::kOS;
 #pragma unroll
-    for (int n = 0; n < D / 8; ++n) {
-      const int c = n * 8 + 2 * q4;
-      sw[g * (D + 2) + 2 + c] = o[n][0];
-      sw[g * (D + 2) + 3 + c] = o[n][1];
-      sw[(g + 8) * (D + 2) + 2 + c] = o[n][2];
-      sw[(g + 8) * (D + 2) + 3 + c] = o[n][3];
+      for (int n = 0; n < D / 8; ++n) {
+        *reinterpret_cast<float2*>(r0p + n * 8) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(r1p + n * 8) = make_float2(o[n][2], o[n][3]);
+      }
     }
     named_sync(2, C::kThreads);
     // ---- merge the warps in order 0..3 and write the split partial
     const int nq = nrows * G;
     for (int e = tid; e < nq * (D / 8); e += C::kThreads) {
       const int qi = e / (D / 8), c0 = (e % (D / 8)) * 8;
-      float mw[C::kWarps], mx = -INFINITY;
+      float2 mlw[C::kWarps];
+      float mx = -INFINITY;
 #pragma unroll
       for (int ww = 0; ww < C::kWarps; ++ww) {
-        mw[ww] = scratch[(ww * 16 + qi) * (D + 2)];
-        mx = fmaxf(mx, mw[ww]);
+        mlw[ww] = sml[ww * 16 + qi];
+        mx = fmaxf(mx, mlw[ww].x);
       }
       float L = 0.0f, acc[8];
 #pragma unroll
@@ -314,12 +319,15 @@ __device__ bool attn_items(const AttnParams& p, const CUtensorMap* kmap_p,
       if (mx != -INFINITY) {
 #pragma unroll
         for (int ww = 0; ww < C::kWarps; ++ww) {
-          if (mw[ww] == -INFINITY) continue;
-          const float sc = exp2f(__fsub_rn(mw[ww], mx));
-          const float* src = scratch + (ww * 16 + qi) * (D + 2);
-          L = __fadd_rn(L, __fmul_rn(src[1], sc));
+          if (mlw[ww].x == -INFINITY) continue;
+          const float sc = exp2f(__fsub_rn(mlw[ww].x, mx));
+          const float* src = so + (ww * 16 + qi) * C::kOS + c0;
+          const float4 v0 = *reinterpret_cast<const float4*>(src);
+          const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+          const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          L = __fadd_rn(L, __fmul_rn(mlw[ww].y, sc));
 #pragma unroll
-          for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(src[2 + c0 + c], sc));
+          for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(vv[c], sc));
         }
       }
       const int r = r0 + qi / G, hq = h * G + qi % G;
