@@ -356,6 +356,70 @@ __device__ void epilogue_logits(const LinParams& p, int tile, float* T, int TS) 
   }
 }
 
+__device__ __forceinline__ unsigned long long tagged(float v) {
+  return (1ull << 32) | __float_as_uint(v);
+}
+
+// Wait (at most kWaitLimitNs) until both words of a pair carry their tag.
+__device__ __forceinline__ bool poll_pair(const unsigned long long* a, unsigned long long& x,
+                                          unsigned long long& y) {
+  if ((x >> 32) != 0 && (y >> 32) != 0) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    ld_relaxed_v2_u64(a, x, y);
+    if ((x >> 32) != 0 && (y >> 32) != 0) return true;
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Reducer side of a split tile: acc holds segment 0 (this CTA's); add the
+// partials that CTAs cta + 1 ... cta + nseg - 1 left in their slots, segment
+// by segment, each thread for the elements its accumulators hold, and clear
+// the words it consumed.  The loads of several segments (six for 8 padded
+// rows) are in flight together, so an exchange whose partials have landed
+// costs one L2 round trip.  Returns false if a partial never arrived.
+template <int MT>
+__device__ __forceinline__ bool gather_partials(unsigned long long* ws, int cta, int nseg, int lr0, int q,
+                                                float (&acc)[MT][4]) {
+  constexpr int MP = MT * 8;
+  constexpr int B = MT == 1 ? 6 : 4 / MT;  // segments in flight (registers: 8 B MT)
+  bool ok = true;
+  for (int j0 = 1; j0 < nseg; j0 += B) {
+    unsigned long long w[B][MT][4];
+#pragma unroll
+    for (int jj = 0; jj < B; ++jj) {
+      if (j0 + jj < nseg) {
+        const unsigned long long* slot = ws + (size_t)(cta + j0 + jj) * kLinRows * MP;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const int m0 = t * 8 + 2 * q;
+          ld_relaxed_v2_u64(slot + lr0 * MP + m0, w[jj][t][0], w[jj][t][1]);
+          ld_relaxed_v2_u64(slot + (lr0 + 8) * MP + m0, w[jj][t][2], w[jj][t][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int jj = 0; jj < B; ++jj) {
+      if (j0 + jj < nseg) {
+        unsigned long long* slot = ws + (size_t)(cta + j0 + jj) * kLinRows * MP;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const int m0 = t * 8 + 2 * q;
+          unsigned long long* a0 = slot + lr0 * MP + m0;
+          unsigned long long* a1 = slot + (lr0 + 8) * MP + m0;
+          if (!poll_pair(a0, w[jj][t][0], w[jj][t][1])) ok = false;
+          if (!poll_pair(a1, w[jj][t][2], w[jj][t][3])) ok = false;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[t][e] = __fadd_rn(acc[t][e], __uint_as_float((uint32_t)w[jj][t][e]));
+          st_relaxed_v2_u64(a0, 0ull, 0ull);
+          st_relaxed_v2_u64(a1, 0ull, 0ull);
+        }
+      }
+    }
+  }
+  return ok;
+}
+
 // Owner of flattened k-block kb under the even split of T k-blocks over G CTAs
 // (CTA c owns [c T / G, (c + 1) T / G)).
 __device__ __forceinline__ int owner_cta(long long kb, long long T, int G) {
@@ -672,65 +736,41 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
     left -= nblk;
     ++tile;
     kk0 = 0;
-    epi_preload<MP, EPI>(p, tile_done, pos, cap, pre);
-    named_sync(1, nthr);  // the previous tile's epilogue is done with T
-    if (kk_first == 0 && kk == KB - 1) {
+    if (kk_first != 0) {
+      // A later segment of a split tile.  It is the first piece of this
+      // CTA's range (every later tile starts at a tile boundary), so a CTA
+      // leaves at most one partial: in its own slot, each value one 64-bit
+      // word with tag 1 in its high half.  The stores are the message: no
+      // fence, no ticket, and nothing waits here.
+      unsigned long long* slot = p.ws + (size_t)cta * kLinRows * MP;
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const int m0 = t * 8 + 2 * q;
-        T[lr0 * TS + m0] = acc[t][0];
-        T[lr0 * TS + m0 + 1] = acc[t][1];
-        T[(lr0 + 8) * TS + m0] = acc[t][2];
-        T[(lr0 + 8) * TS + m0 + 1] = acc[t][3];
+        st_relaxed_v2_u64(slot + lr0 * MP + m0, tagged(acc[t][0]), tagged(acc[t][1]));
+        st_relaxed_v2_u64(slot + (lr0 + 8) * MP + m0, tagged(acc[t][2]), tagged(acc[t][3]));
+        acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
       }
-    } else {
-      const int c_first = owner_cta((long long)tile_done * KB, Tk, G);
-      const int c_last = owner_cta((long long)tile_done * KB + KB - 1, Tk, G);
-      const int nseg = c_last - c_first + 1, seg = cta - c_first;
-      float* wsb = p.ws + ((size_t)(tile_done * p.max_seg + seg) * kLinRows) * MP;
-#pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        const int m0 = t * 8 + 2 * q;
-        *reinterpret_cast<float2*>(wsb + lr0 * MP + m0) = make_float2(acc[t][0], acc[t][1]);
-        *reinterpret_cast<float2*>(wsb + (lr0 + 8) * MP + m0) = make_float2(acc[t][2], acc[t][3]);
-      }
-      named_sync(1, nthr);
-      if (tid == 0) {
-        // one acq_rel ticket: releases this CTA's partial (the barrier before
-        // it makes the other threads' stores part of it) and acquires those
-        // of the CTAs that arrived before
-        unsigned prev;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                     : "=r"(prev)
-                     : "l"(reinterpret_cast<unsigned*>(p.counters + tile_done))
-                     : "memory");
-        *sm.s_flag = (prev == (unsigned)(nseg - 1));
-      }
-      named_sync(1, nthr);
-      const bool last = *sm.s_flag != 0;
-      if (last) {
-        // last CTA of this tile: sum the partials of its CTAs in k order
-        const float* wst = p.ws + ((size_t)tile_done * p.max_seg * kLinRows) * MP;
-        for (int e = tid; e < kLinRows * p.M; e += nthr) {
-          const int lr = e / p.M, m = e % p.M;
-          float part[kLinMaxSeg];
-#pragma unroll
-          for (int j = 0; j < kLinMaxSeg; ++j)
-            if (j < nseg) part[j] = __ldcg(wst + ((size_t)j * kLinRows + lr) * MP + m);
-          float v = part[0];
-#pragma unroll
-          for (int j = 1; j < kLinMaxSeg; ++j)
-            if (j < nseg) v = __fadd_rn(v, part[j]);
-          T[lr * TS + m] = v;
-        }
-        if (tid == 0) p.counters[tile_done] = 0;  // ready for the next use
-      }
-#pragma unroll
-      for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
-      if (!last) continue;
+      continue;
     }
+    epi_preload<MP, EPI>(p, tile_done, pos, cap, pre);
+    if (kk != KB - 1) {
+      // The first segment of a split tile: the last piece of this CTA's
+      // range, so waiting here holds up no stream.  The other segments belong
+      // to CTAs cta + 1 ... c_last, in k order; add their partials in that
+      // order (the same sums, in the same order, whichever CTAs ran them).
+      const int nseg = owner_cta((long long)tile_done * KB + KB - 1, Tk, G) - cta + 1;
+      if (!gather_partials<MT>(p.ws, cta, nseg, lr0, q, acc)) ok = false;
+    }
+    named_sync(1, nthr);  // the previous tile's epilogue is done with T
 #pragma unroll
-    for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    for (int t = 0; t < MT; ++t) {
+      const int m0 = t * 8 + 2 * q;
+      T[lr0 * TS + m0] = acc[t][0];
+      T[lr0 * TS + m0 + 1] = acc[t][1];
+      T[(lr0 + 8) * TS + m0] = acc[t][2];
+      T[(lr0 + 8) * TS + m0 + 1] = acc[t][3];
+      acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+    }
     named_sync(1, nthr);
     if (EPI == EPI_QKV)
       epilogue_qkv<MP>(p, tile_done, T, TS, sm.s_hrstd, pos, pre);

@@ -47,8 +47,7 @@ struct sv_ctx {
   float2* part_ml = nullptr;
   float* part_o = nullptr;
   int max_splits = 0;
-  float* ws = nullptr;
-  int* counters = nullptr;
+  unsigned long long* ws = nullptr;  // split-tile partial slots, one per CTA (tags start at 0)
   float* am_val = nullptr;
   int* am_idx = nullptr;
   // pinned host staging
@@ -162,7 +161,6 @@ LinParams lin_params(sv_ctx* ctx, int which, int l, int M, int mode, float* logi
   p.ffn = c.ffn;
   p.head_dim = d;
   p.ws = ctx->ws;
-  p.counters = ctx->counters;
   p.block_table = ctx->block_table;
   p.rope = ctx->rope;
   p.n_q_heads = Hq;
@@ -497,11 +495,9 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   ctx->layer_stride = (size_t)c.max_pages * Hkv * kPage * d;
   const size_t pool = ctx->layer_stride * (L > 0 ? L : 1);
   ctx->max_splits = (c.max_seq + kAttnSplit - 1) / kAttnSplit;
-  size_t ws_floats = 0;
-  int max_tiles = ctx->lin_head.n_tiles;
+  size_t ws_words = 0;
   auto acc_ws = [&](const LinearDesc& ld) {
-    if (ld.max_seg > 1) ws_floats = std::max(ws_floats, (size_t)ld.n_tiles * ld.max_seg * kLinRows * MP);
-    max_tiles = std::max(max_tiles, ld.n_tiles);
+    if (ld.max_seg > 1) ws_words = std::max(ws_words, (size_t)ld.grid * kLinRows * MP);
   };
   for (int l = 0; l < L; ++l) {
     acc_ws(ctx->lin_qkv[l]);
@@ -520,7 +516,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->rope, (size_t)c.max_seq * (d / 2))) ||
       (rc = dalloc(ctx, &ctx->part_ml, (size_t)c.max_k * Hq * ctx->max_splits)) ||
       (rc = dalloc(ctx, &ctx->part_o, (size_t)c.max_k * Hq * ctx->max_splits * d)) ||
-      (rc = dalloc(ctx, &ctx->ws, ws_floats)) || (rc = dalloc(ctx, &ctx->counters, (size_t)max_tiles)) ||
+      (rc = dalloc(ctx, &ctx->ws, ws_words)) ||
       (rc = dalloc(ctx, &ctx->am_val, (size_t)kMaxK * ctx->lin_head.n_tiles)) ||
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
@@ -716,7 +712,6 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
   base.ffn = c.ffn;
   base.head_dim = c.head_dim;
   base.ws = ctx->ws;
-  base.counters = ctx->counters;
   base.n_q_heads = c.n_q_heads;
   base.n_kv_heads = c.n_kv_heads;
   base.act = c.act;

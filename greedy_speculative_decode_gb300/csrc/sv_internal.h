@@ -71,8 +71,10 @@ struct LinParams {
   float eps;
   int M, Kd, n_tiles, max_seg, map, ffn, head_dim;
   int grid;      // CTAs the weight is divided over (one per SM, at most one per k-block)
-  float* ws;     // partial tiles of tiles shared by several CTAs: [n_tiles][max_seg][128][MP]
-  int* counters; // one ticket per tile
+  // split-tile partials, one slot per CTA: [grid][128][MP] words {fp32 bits,
+  // tag}; a CTA whose range starts inside a tile leaves its partial of that
+  // tile in its slot (tag 1), the tile's first CTA adds it and clears it (0)
+  unsigned long long* ws;
   // epilogue operands
   bf16* out;           // EPI_QKV: q [M, Hq d]; EPI_RESID: x [M, N] (in place); EPI_GLU: a [M, ffn]
   int out_stride;

@@ -113,11 +113,11 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   const int mp = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const size_t off_state = 0;
   const size_t off_ss = round256(off_state + sizeof(SvState));
-  const size_t off_cnt = round256(off_ss + sizeof(float) * (size_t)M * (hidden / 128));
-  const size_t off_amv = round256(off_cnt + sizeof(int) * (size_t)n_tiles);
+  const size_t off_amv = round256(off_ss + sizeof(float) * (size_t)M * (hidden / 128));
   const size_t off_ami = round256(off_amv + sizeof(float) * (size_t)M * n_tiles);
   const size_t off_ws = round256(off_ami + sizeof(int) * (size_t)M * n_tiles);
-  const size_t end = off_ws + (max_seg > 1 ? sizeof(float) * (size_t)n_tiles * max_seg * kLinRows * mp : 0);
+  const size_t ws_bytes = max_seg > 1 ? sizeof(unsigned long long) * (size_t)grid * kLinRows * mp : 0;
+  const size_t end = off_ws + ws_bytes;
   if (end > kNoAllocScratchBytes) return SV_E_NOMEM;  // larger than the fixed array
 
   {
@@ -134,10 +134,9 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   unsigned char* base = static_cast<unsigned char*>(g_setup[dev].base);
   SvState* st = reinterpret_cast<SvState*>(base + off_state);
   float* x_ss = reinterpret_cast<float*>(base + off_ss);
-  int* counters = reinterpret_cast<int*>(base + off_cnt);
   float* am_val = reinterpret_cast<float*>(base + off_amv);
   int* am_idx = reinterpret_cast<int*>(base + off_ami);
-  float* ws = reinterpret_cast<float*>(base + off_ws);
+  unsigned long long* ws = reinterpret_cast<unsigned long long*>(base + off_ws);
 
   // Tensor map of the weight: a host-side encoding, no device memory.
   void* enc_fn = nullptr;
@@ -166,10 +165,10 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   }
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  // What must start at zero: the status word and the split tickets (a call
-  // that stopped early could have left them set).
+  // What must start at zero: the status word and the tags of the split-tile
+  // partial slots (a call that stopped early could have left them set).
   if (cudaMemsetAsync(st, 0, sizeof(SvState), s) != cudaSuccess ||
-      cudaMemsetAsync(counters, 0, sizeof(int) * (size_t)n_tiles, s) != cudaSuccess)
+      (ws_bytes > 0 && cudaMemsetAsync(ws, 0, ws_bytes, s) != cudaSuccess))
     return SV_E_CUDA;
   k_rows_ss<<<dim3(hidden / 128, M), 128, 0, s>>>(static_cast<const bf16*>(x_dev), hidden, x_ss,
                                                   hidden / 128);
@@ -188,7 +187,6 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   p.grid = grid;
   p.map = MAP_PLAIN;
   p.ws = ws;
-  p.counters = counters;
   p.logits = logits_dev;
   p.logits_row0 = 0;
   p.am_val = am_val;

@@ -182,13 +182,13 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
  *   argmax_dev: int32 [M] or NULL; status_dev: int32 [1] or NULL, set to 0, or
  *     to the kernels' failure bits (1 timeout).
  *   cuda_stream: the stream to run on (NULL = legacy stream).  Asynchronous.
- * Scratch: the split-K partial tiles, their tickets, the argmax partials and
+ * Scratch: the split-K partials (one slot per CTA), the argmax partials and
  * the row statistics live in one fixed 8 MiB device array inside the library
  * (held on every GPU that loads it until the process exits).  Shapes whose
- * scratch would not fit return SV_E_NOMEM; the bound is about
- *   4 * ceil(vocab/128) * S * 128 * (8, 16 or 32 for M <= 8, 16, 32) bytes
- *   <= 8 MiB, where S (1 or 2 for usual shapes) is the most CTAs that one
- *   128-row slice of W is divided over (one CTA per SM, equal shares of W).
+ * scratch would not fit return SV_E_NOMEM; the scratch is about
+ *   8 * M * ceil(vocab/128) + 8 * G * 128 * (8, 16 or 32 for M <= 8, 16, 32)
+ *   bytes, G <= the SM count (one CTA per SM, equal shares of W): with 152
+ *   SMs a vocabulary of up to about 1.7 million ids fits at any M.
  * Other limits: 1 <= M <= 32, hidden % 128 == 0 (else SV_E_INVAL).
  * The first call on a device looks up the array's address and sets kernel
  * attributes for that device; make that first call before any stream capture.

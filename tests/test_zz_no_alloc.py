@@ -54,12 +54,22 @@ def test_no_alloc_lm_head_matches_context_wide():
     _compare(cfg, [11, 2049, 30000, 7], seed=4)
 
 
+def test_no_alloc_lm_head_matches_context_full_vocab():
+    """The 151,936-id vocabulary of the 8B-shaped model (1187 tiles, split
+    tiles between neighbouring CTAs) fits the fixed scratch."""
+    cfg = inputs.shrink(inputs.QWEN3_8B, n_layers=0)
+    _compare(cfg, [3, 151935, 70000, 12, 99999], seed=6)
+
+
 def test_no_alloc_rejects_shapes_beyond_the_scratch():
+    """32 rows of a 2,000,000-id vocabulary: the argmax partials alone
+    (8 bytes per row per 128-id tile) take 4 MB, the partial slots 5 MB."""
     import greedy_speculative_decode_gb300 as sv
-    x = torch.zeros((4, 4096), dtype=torch.bfloat16, device="cuda")
-    g = torch.ones((4096,), dtype=torch.bfloat16, device="cuda")
-    w = torch.zeros((151936, 4096), dtype=torch.bfloat16, device="cuda")
-    lg = torch.empty((4, 151936), dtype=torch.float32, device="cuda")
+    V = 2_000_000
+    x = torch.zeros((32, 128), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones((128,), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((V, 128), dtype=torch.bfloat16, device="cuda")
+    lg = torch.empty((32, V), dtype=torch.float32, device="cuda")
     with pytest.raises(sv.SvError) as e:
         sv.lm_head_noalloc(x, g, w, lg)
     assert e.value.code == sv.SV_E_NOMEM
