@@ -356,64 +356,44 @@ __device__ void epilogue_logits(const LinParams& p, int tile, float* T, int TS) 
   }
 }
 
-__device__ __forceinline__ unsigned long long tagged(float v) {
-  return (1ull << 32) | __float_as_uint(v);
-}
-
-// Wait (at most kWaitLimitNs) until both words of a pair carry their tag.
-__device__ __forceinline__ bool poll_pair(const unsigned long long* a, unsigned long long& x,
-                                          unsigned long long& y) {
-  if ((x >> 32) != 0 && (y >> 32) != 0) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    ld_relaxed_v2_u64(a, x, y);
-    if ((x >> 32) != 0 && (y >> 32) != 0) return true;
-    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // Reducer side of a split tile: acc holds segment 0 (this CTA's); add the
 // partials that CTAs cta + 1 ... cta + nseg - 1 left in their slots, segment
 // by segment, each thread for the elements its accumulators hold, and clear
-// the words it consumed.  The loads of several segments (six for 8 padded
-// rows) are in flight together, so an exchange whose partials have landed
-// costs one L2 round trip.  Returns false if a partial never arrived.
+// the words it consumed.  The words of several segments (six for 8 padded
+// rows) are requested together and polled in rounds, so an exchange costs one
+// L2 round trip once the partials have landed.  Returns false if a partial
+// never arrived.
 template <int MT>
 __device__ __forceinline__ bool gather_partials(unsigned long long* ws, int cta, int nseg, int lr0, int q,
                                                 float (&acc)[MT][4]) {
   constexpr int MP = MT * 8;
   constexpr int B = MT == 1 ? 6 : 4 / MT;  // segments in flight (registers: 8 B MT)
+  constexpr int NP = B * MT * 2;           // word pairs per thread and batch
   bool ok = true;
   for (int j0 = 1; j0 < nseg; j0 += B) {
-    unsigned long long w[B][MT][4];
+    // pair i = (segment j0 + i / (2 MT), accumulator t = (i / 2) % MT, row half i % 2)
+    auto addr = [&](int i) {
+      const int jj = i / (2 * MT), t = (i / 2) % MT, half = i % 2;
+      return ws + (size_t)(cta + j0 + jj) * kLinRows * MP + (lr0 + 8 * half) * MP + t * 8 + 2 * q;
+    };
+    unsigned long long x[NP], y[NP];
+    uint32_t live = 0;
 #pragma unroll
-    for (int jj = 0; jj < B; ++jj) {
-      if (j0 + jj < nseg) {
-        const unsigned long long* slot = ws + (size_t)(cta + j0 + jj) * kLinRows * MP;
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const int m0 = t * 8 + 2 * q;
-          ld_relaxed_v2_u64(slot + lr0 * MP + m0, w[jj][t][0], w[jj][t][1]);
-          ld_relaxed_v2_u64(slot + (lr0 + 8) * MP + m0, w[jj][t][2], w[jj][t][3]);
-        }
+    for (int i = 0; i < NP; ++i) {
+      x[i] = y[i] = 0ull;
+      if (j0 + i / (2 * MT) < nseg) {
+        live |= 1u << i;
+        ld_relaxed_v2_u64(addr(i), x[i], y[i]);
       }
     }
+    if (!poll_pairs<NP>(addr, x, y, live)) ok = false;
 #pragma unroll
-    for (int jj = 0; jj < B; ++jj) {
-      if (j0 + jj < nseg) {
-        unsigned long long* slot = ws + (size_t)(cta + j0 + jj) * kLinRows * MP;
-#pragma unroll
-        for (int t = 0; t < MT; ++t) {
-          const int m0 = t * 8 + 2 * q;
-          unsigned long long* a0 = slot + lr0 * MP + m0;
-          unsigned long long* a1 = slot + (lr0 + 8) * MP + m0;
-          if (!poll_pair(a0, w[jj][t][0], w[jj][t][1])) ok = false;
-          if (!poll_pair(a1, w[jj][t][2], w[jj][t][3])) ok = false;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[t][e] = __fadd_rn(acc[t][e], __uint_as_float((uint32_t)w[jj][t][e]));
-          st_relaxed_v2_u64(a0, 0ull, 0ull);
-          st_relaxed_v2_u64(a1, 0ull, 0ull);
-        }
+    for (int i = 0; i < NP; ++i) {
+      if ((live >> i) & 1u) {
+        const int t = (i / 2) % MT, half = i % 2;
+        acc[t][2 * half] = __fadd_rn(acc[t][2 * half], __uint_as_float((uint32_t)x[i]));
+        acc[t][2 * half + 1] = __fadd_rn(acc[t][2 * half + 1], __uint_as_float((uint32_t)y[i]));
+        st_relaxed_v2_u64(addr(i), 0ull, 0ull);
       }
     }
   }
