@@ -26,16 +26,18 @@ namespace sv {
 
 namespace {
 
-template <int D>
+// kMulti: the form for grids whose CTAs run several work items (long
+// contexts), which requests each CTA's next item while it merges this one.
+template <int D, bool kMulti>
 __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
     k_attention(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                 const AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  AttnSmem<D> sm;
+  AttnSmem<D, kMulti> sm;
   sm.carve(smem);
-  if (threadIdx.x == 0) attn_init_bars<D>(sm);
+  if (threadIdx.x == 0) attn_init_bars<D, kMulti>(sm);
   __syncthreads();
   pdl_trigger();
   // The committed length is final for the whole step (only the step's last
@@ -44,10 +46,18 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
   // the cache pages that earlier steps wrote.
   const int pos = __ldcg(&p.st->seq_len);
   uint32_t phase = 0;
-  if (!attn_items<D>(p, &kmap, &vmap, blockIdx.x, gridDim.x, sm, phase, pos) && (threadIdx.x & 31) == 0)
+  bool ok;
+  if constexpr (kMulti)
+    ok = attn_items_multi<D>(p, &kmap, &vmap, blockIdx.x, gridDim.x, sm, phase, pos);
+  else
+    ok = attn_items_single<D>(p, &kmap, &vmap, blockIdx.x, gridDim.x, sm, phase, pos);
+  if (!ok && (threadIdx.x & 31) == 0)
     atomicOr(&p.st->status, ST_TIMEOUT);
 }
 
+// One block per (row, query head), one thread per element.  Contexts of at
+// most eight splits use this light form (few registers, so its blocks fit
+// beside the attention kernel's and are resident before it ends).
 template <int D>
 __global__ void __launch_bounds__(D) k_attn_combine(const AttnParams p) {
   pdl_trigger();
@@ -56,11 +66,29 @@ __global__ void __launch_bounds__(D) k_attn_combine(const AttnParams p) {
                      __ldcg(&p.st->step_pos));
 }
 
+// Longer contexts: rows of more than eight splits take combine_long.
+// Dynamic shared memory: the (m, l) pairs of up to max_splits splits.
+// (Its register cap lets its blocks fit beside an attention block.)
 template <int D>
+__global__ void __launch_bounds__(D, 768 / D) k_attn_combine_long(const AttnParams p) {
+  extern __shared__ float2 s_ml[];
+  __shared__ float s_red[D / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x / p.n_q_heads, hq = blockIdx.x % p.n_q_heads;
+  const int pos = __ldcg(&p.st->step_pos);
+  const int ns = (pos + r + kAttnSplit) / kAttnSplit;  // splits row r sees
+  if (ns <= 8)
+    combine_element<D>(p, r, hq, threadIdx.x, pos);
+  else
+    combine_long<D>(p, r, hq, ns, s_ml, s_red);
+}
+
+template <int D, bool kMulti>
 cudaError_t launch_attn_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
                           int grid, cudaStream_t s, bool pdl) {
-  const int smem = AttnCfg<D>::kSmem;
-  auto kern = k_attention<D>;
+  const int smem = AttnSmem<D, kMulti>::kSmem;
+  auto kern = k_attention<D, kMulti>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(AttnCfg<D>::kThreads);
@@ -79,35 +107,48 @@ cudaError_t launch_comb_t(const AttnParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.M * p.n_q_heads);
   cfg.blockDim = dim3(D);
+  const bool long_ctx = p.max_splits > 8;
+  cfg.dynamicSmemBytes = long_ctx ? (size_t)p.max_splits * sizeof(float2) : 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_attn_combine<D>, p);
+  return long_ctx ? cudaLaunchKernelEx(&cfg, k_attn_combine_long<D>, p)
+                  : cudaLaunchKernelEx(&cfg, k_attn_combine<D>, p);
+}
+
+
+template <int D, bool kMulti>
+cudaError_t prepare_attn_t() {
+  return cudaFuncSetAttribute(k_attention<D, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              AttnSmem<D, kMulti>::kSmem);
 }
 
 }  // namespace
 
 cudaError_t prepare_attention_kernels() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(k_attention<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                AttnCfg<64>::kSmem)) != cudaSuccess)
+  if ((e = prepare_attn_t<64, false>()) != cudaSuccess || (e = prepare_attn_t<64, true>()) != cudaSuccess ||
+      (e = prepare_attn_t<128, false>()) != cudaSuccess || (e = prepare_attn_t<128, true>()) != cudaSuccess ||
+      (e = prepare_attn_t<256, false>()) != cudaSuccess)
     return e;
-  if ((e = cudaFuncSetAttribute(k_attention<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                AttnCfg<128>::kSmem)) != cudaSuccess)
-    return e;
-  return cudaFuncSetAttribute(k_attention<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              AttnCfg<256>::kSmem);
+  return prepare_attn_t<256, true>();
 }
 
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
-                             int head_dim, int grid, cudaStream_t s, bool pdl) {
+                             int head_dim, int grid, bool multi, cudaStream_t s, bool pdl) {
   switch (head_dim) {
-    case 64: return launch_attn_t<64>(kmap, vmap, p, grid, s, pdl);
-    case 128: return launch_attn_t<128>(kmap, vmap, p, grid, s, pdl);
-    case 256: return launch_attn_t<256>(kmap, vmap, p, grid, s, pdl);
+    case 64:
+      return multi ? launch_attn_t<64, true>(kmap, vmap, p, grid, s, pdl)
+                   : launch_attn_t<64, false>(kmap, vmap, p, grid, s, pdl);
+    case 128:
+      return multi ? launch_attn_t<128, true>(kmap, vmap, p, grid, s, pdl)
+                   : launch_attn_t<128, false>(kmap, vmap, p, grid, s, pdl);
+    case 256:
+      return multi ? launch_attn_t<256, true>(kmap, vmap, p, grid, s, pdl)
+                   : launch_attn_t<256, false>(kmap, vmap, p, grid, s, pdl);
   }
   return cudaErrorInvalidValue;
 }

@@ -255,7 +255,9 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, s));
   const int G = c.n_q_heads / Hkv;
   const int n_rb = (M + kAttnQ / G - 1) / (kAttnQ / G);
-  const int attn_grid = std::max(1, std::min(ctx->max_splits * Hkv * n_rb, ctx->num_sms));
+  const int attn_items_max = ctx->max_splits * Hkv * n_rb;  // attention work items at max_seq
+  const int attn_grid = std::max(1, std::min(attn_items_max, ctx->num_sms));
+  const bool attn_multi = attn_items_max > attn_grid;
   int epi;
   bool norm;
   const LinearDesc* ld;
@@ -279,7 +281,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
     LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
     CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_QKV, l)));
     AttnParams ap = attn_params(ctx, l, M);
-    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, s, ctx->use_pdl));
+    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, ctx->use_pdl));
     CK(launch_attn_combine(ap, d, s, ctx->use_pdl));
     for (int w : {LIN_O, LIN_GU, LIN_DOWN}) {
       p = lin_params(ctx, w, l, M, mode, logits, &epi, &norm, &ld);
@@ -419,7 +421,7 @@ int validate(const sv_config* c) {
   if (c->qk_norm && c->head_dim > 128) return 0;
   if (c->act != 0 && c->act != 1) return 0;
   if (c->page_size != kPage || c->max_k < 1 || c->max_k > kMaxK) return 0;
-  if (c->max_seq < c->max_k || c->max_pages < 1) return 0;
+  if (c->max_seq < c->max_k || c->max_seq > kMaxSeq || c->max_pages < 1) return 0;
   return 1;
 }
 

@@ -38,6 +38,9 @@ constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;  // consumers, then th
 
 // Attention geometry: a split is 256 absolute positions = 4 warps x 4 pages.
 constexpr int kAttnSplit = 256;  // positions per split (split s: [256 s, 256 s + 256))
+// Longest sequence a context may hold: the split merge stages the (m, l)
+// pairs of every split in shared memory (8 bytes each, 32 KB at this bound).
+constexpr int kMaxSeq = 1 << 20;
 constexpr int kAttnQ = 16;  // query rows (token rows x heads of one group) per work item
 
 // Kinds of linear epilogue.
@@ -125,8 +128,9 @@ cudaError_t prepare_attention_kernels();
 cudaError_t launch_linear(const LinearDesc& d, const LinParams& p, int epi, bool norm,
                           cudaStream_t s, bool pdl, const LinearDesc* next = nullptr);
 size_t linear_smem_bytes(int mt);
+// multi: some CTA of the grid runs more than one work item (long contexts)
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
-                             int head_dim, int grid, cudaStream_t s, bool pdl);
+                             int head_dim, int grid, bool multi, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_combine(const AttnParams& p, int head_dim, cudaStream_t s, bool pdl);
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
                          SvState* st, cudaStream_t s);

@@ -60,8 +60,8 @@ typedef struct sv_ctx sv_ctx;
  *   n_q_heads % n_kv_heads == 0 and 16 % (n_q_heads / n_kv_heads) == 0.
  *   act: 0 = SwiGLU silu(gate)*up, 1 = GeGLU with tanh-approximated GELU.
  *   page_size must be 16.  max_k in [1, 32].  max_seq: longest sequence
- *   (committed + window); max_pages: KV pool size in pages (>= max_seq/16 for
- *   one full sequence). */
+ *   (committed + window), in [max_k, 1048576]; max_pages: KV pool size in
+ *   pages (>= max_seq/16 for one full sequence). */
 typedef struct {
   int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
   float rms_eps, rope_theta;
