@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="use only the first N layers of the model (profiling cases)")
     ap.add_argument("--vocab", type=int, default=None, help="override the vocabulary size")
+    ap.add_argument("--spec", action="store_true",
+                    help="time the draft -> verify loop against plain decoding (separate JSON line)")
     ap.add_argument("--linear-only", action="store_true",
                     help="time each linear class once per layer (NVTX range 'linear') and exit")
     return ap.parse_args()
@@ -306,12 +308,108 @@ def run_linear_only(args):
                       "linears": out}))
 
 
+def audit(steps, first, count, every, prefix, K, vocab):
+    """Low-rate verify audit: for every `every`-th of the steps first ..
+    first + count - 1, every row of the verify logits against the
+    single-token decode logits after the same tokens, bit for bit.  Row r of
+    a window [t0, d1, .., d_{K-1}] at committed length L must equal decode's
+    logits after feeding t0, d1, .., d_r from L.  On a mismatch the top 5
+    (id, logit) of both sides are kept (the first three)."""
+    import torch
+    lv = torch.empty((K, vocab), dtype=torch.float32, device="cuda")
+    ld = torch.empty((1, vocab), dtype=torch.float32, device="cuda")
+    rows = equal = 0
+    examples = []
+    top5 = lambda x: [[int(a), float(b)] for a, b in zip(*(t.tolist() for t in torch.topk(x, 5)[::-1]))]
+    for j in range(first, first + count, every):
+        sq, i, toks, _ = steps[j]
+        ctx, base = sq["ctx"], prefix + i
+        if len(ctx) > base:
+            ctx.truncate(base)
+        elif len(ctx) < base:  # commit the chain up to the step's prefix
+            ctx.prefill(sq["chain"][len(ctx) - prefix:i])
+        ctx.verify(toks, lv)
+        ctx.truncate(base)
+        for r, t in enumerate(toks):
+            ctx.decode(t, ld)
+            rows += 1
+            if torch.equal(lv[r], ld[0]):
+                equal += 1
+            elif len(examples) < 3:
+                examples.append({"step": j, "row": r, "max_abs_diff": float((lv[r] - ld[0]).abs().max()),
+                                 "verify_top5": top5(lv[r]), "decode_top5": top5(ld[0])})
+        ctx.truncate(base)
+    return {"every": every, "rows": rows, "bitwise_equal": equal, "mismatches": examples}
+
+
+def run_spec(args):
+    """Draft -> verify loop (sv_spec_generate) against plain decoding on the
+    target, wall clock around synchronous calls, prompt prefill excluded.
+    Drafters: a random-init 0.6B-shaped model (seed 1, its own weights: it
+    rarely agrees with the target) and the target's own weights (it always
+    does: every draft accepted, K tokens per verify step)."""
+    import torch
+
+    import greedy_speculative_decode_gb300 as sv
+    cfg = model_config(args)
+    K, n_new, reps = args.K, GEN_TOKENS, 3
+    tw = inputs.device_weights(cfg, seed=0, gain_std=0.0)
+    small = inputs.shrink(inputs.QWEN3_0P6B, vocab=cfg.vocab)
+    sw = inputs.device_weights(small, seed=1, gain_std=0.0)
+    max_seq = args.prefix + n_new + 2 * K + 8
+    prompt = inputs.prefix_tokens(0, args.prefix, cfg.vocab)
+    tgt = sv.Context(cfg, tw, max_k=max(K, 8), max_seq=max_seq)
+    pending = tgt.prefill(prompt)
+
+    def timed(fn):
+        best = None
+        for r in range(reps + 1):  # the first pass warms up (graphs, pages)
+            tgt.truncate(args.prefix)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            out = fn()
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            if r > 0:
+                best = dt if best is None else min(best, dt)
+        return out, best
+
+    def decode_only():
+        t, toks = pending, []
+        for _ in range(n_new):
+            toks.append(t)
+            t = tgt.decode(t)
+        return toks
+
+    ref, t_dec = timed(decode_only)
+    out = {"mode": "spec", "target": cfg.name, "K": K, "prefix": args.prefix, "tokens": n_new,
+           "decode_tok_s": n_new / t_dec, "drafters": {}}
+    for name, dcfg, dw in (("0.6b-shape random", small, sw), ("target itself", cfg, tw)):
+        drf = sv.Context(dcfg, dw, max_k=max(K, 8), max_seq=max_seq)
+        drf.prefill(prompt)
+
+        def spec():
+            drf.truncate(args.prefix)
+            return sv.spec_generate(tgt, drf, pending, K, n_new)
+
+        (toks, _, st), t_spec = timed(spec)
+        assert toks[:n_new] == ref, f"{name}: speculative output differs from greedy decoding"
+        out["drafters"][name] = {
+            "tok_s": len(toks) / t_spec, "speedup_vs_decode": (len(toks) / t_spec) / (n_new / t_dec),
+            "acceptance_rate": st["accepted"] / max(1, st["proposed"]),
+            "tokens_per_verify_step": len(toks) / st["verify_steps"], "output_equals_greedy": True}
+        drf.close()
+    print(json.dumps(out))
+
+
 def run_ours(args):
     import torch
 
     import greedy_speculative_decode_gb300 as sv
     if args.linear_only:
         return run_linear_only(args)
+    if args.spec:
+        return run_spec(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -404,6 +502,9 @@ def run_ours(args):
     lin = {w: ctx0.time_linear(code, K, reps=3) for w, code in
            (("o", sv.SV_LIN_O), ("down", sv.SV_LIN_DOWN), ("lm_head", sv.SV_LIN_LM_HEAD))}
 
+    # ---------------- low-rate audit of verify rows against single-token decode
+    aud = audit(steps, W, S, max(1, S // 8), args.prefix, K, cfg.vocab)
+
     mean_pos = pos_sum / S
     sb = step_bytes(cfg, K, mean_pos)
     ms_per_step = dev_ms / S
@@ -425,6 +526,7 @@ def run_ours(args):
         **{k: v for k, v in counters(accepted, proposed, tokens, S, dev_ms / 1000.0).items()
            if k in ("acceptance_rate", "tokens_per_target_step")},
         "verify_decode_mismatches": mismatches,
+        "verify_audit": aud,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": ncu_traffic(),
                      "kernel": "k_linear (gate|up + SwiGLU epilogue)", "peak_kind": peak_kind,

@@ -63,6 +63,7 @@ def _load():
     L.sv_kv_read.argtypes = [_P, _i32, _i32, _i32, _P, _P]
     L.sv_shuffle_pages.argtypes = [_P, ctypes.c_uint64]
     L.sv_step_kernel_count.argtypes = [_P, _i32, _i32]
+    L.sv_spec_generate.argtypes = [_P, _P, _i32, _i32, _i32, _P, _P, _P, _P]
     L.sv_time_linear.argtypes = [_P, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_float),
                                  ctypes.POINTER(ctypes.c_double)]
     L.sv_lm_head_noalloc.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_float, _P, _P, _P, _P]
@@ -106,6 +107,20 @@ def lm_head_noalloc(x, gain, w, logits, argmax=None, status=None, eps=1e-6, stre
     if rc != SV_OK:
         raise SvError(rc, "sv_lm_head_noalloc rejected the shapes (scratch limit 8 MiB, "
                           "1 <= M <= 32, hidden % 128 == 0) or a CUDA call failed")
+
+
+def spec_generate(target: "Context", draft: "Context", pending: int, K: int, n_new: int):
+    """sv_spec_generate: greedy speculative generation of at least n_new tokens
+    from `pending`, drafted by `draft` and verified by `target` (both holding
+    the same tokens).  Returns (tokens committed, next pending token,
+    {"verify_steps", "accepted", "proposed"})."""
+    out = (ctypes.c_int32 * (n_new + max(K, 1) - 1))()
+    n_out, nxt = ctypes.c_int32(0), ctypes.c_int32(0)
+    stats = (ctypes.c_int32 * 3)()
+    target._check(_lib.sv_spec_generate(target._h, draft._h, int(pending), int(K), int(n_new), out,
+                                        ctypes.byref(n_out), ctypes.byref(nxt), stats))
+    return (list(out[:n_out.value]), nxt.value,
+            {"verify_steps": stats[0], "accepted": stats[1], "proposed": stats[2]})
 
 
 class Context:

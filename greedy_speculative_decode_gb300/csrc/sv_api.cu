@@ -693,6 +693,57 @@ int sv_shuffle_pages(sv_ctx* ctx, uint64_t seed) {
   return SV_OK;
 }
 
+int sv_spec_generate(sv_ctx* target, sv_ctx* draft, int32_t pending, int K, int n_new,
+                     int32_t* out_tokens, int32_t* n_out, int32_t* next_pending, int32_t* stats) {
+  if (!target || !draft || target == draft) return SV_E_INVAL;
+  const sv_config& tc = target->cfg;
+  if (n_new < 1 || !out_tokens || !n_out || !next_pending || K < 1 || K > tc.max_k)
+    return fail(target, SV_E_INVAL, "sv_spec_generate(K=%d, n_new=%d)", K, n_new);
+  if (pending < 0 || pending >= tc.vocab)
+    return fail(target, SV_E_INVAL, "pending token %d out of range [0, %d)", pending, tc.vocab);
+  if (draft->cfg.vocab != tc.vocab)
+    return fail(target, SV_E_INVAL, "drafter vocabulary %d differs from the target's %d", draft->cfg.vocab,
+                tc.vocab);
+  if (target->async_pending || draft->async_pending || target->seq_len != draft->seq_len)
+    return fail(target, SV_E_STATE, "sv_spec_generate needs two synchronised contexts of equal length");
+  const long long need = (long long)target->seq_len + n_new + K;
+  if (need > tc.max_seq || need > draft->cfg.max_seq)
+    return fail(target, SV_E_INVAL, "length + n_new + K = %lld exceeds max_seq", need);
+  // a drafter call that fails reports through the target's error message
+  auto drafter = [&](int code) { return fail(target, code, "drafter: %s", draft->err.c_str()); };
+  int rc;
+  int32_t ignored = 0;
+  std::vector<int32_t> block(K);
+  int produced = 0, steps = 0, accepted = 0, proposed = 0;
+  while (produced < n_new) {
+    const int base = target->seq_len;  // == draft->seq_len
+    block[0] = pending;
+    for (int j = 1; j < K; ++j)  // the drafter commits block[j - 1] and proposes block[j]
+      if ((rc = sv_decode(draft, block[j - 1], nullptr, &block[j])) != SV_OK) return drafter(rc);
+    int32_t n = 0, corr = 0;
+    if ((rc = sv_verify(target, block.data(), K, nullptr, &n, &corr)) != SV_OK) return rc;
+    ++steps;
+    accepted += n;
+    proposed += K - 1;
+    for (int j = 0; j <= n; ++j) out_tokens[produced++] = block[j];
+    // the drafter holds block[0 .. K-2]; the target committed block[0 .. n]
+    if (n + 1 < K - 1) {
+      if ((rc = sv_truncate(draft, base + n + 1)) != SV_OK) return drafter(rc);
+    } else if (n + 1 == K) {
+      if ((rc = sv_prefill(draft, &block[K - 1], 1, nullptr, &ignored)) != SV_OK) return drafter(rc);
+    }
+    pending = corr;
+  }
+  *n_out = produced;
+  *next_pending = pending;
+  if (stats) {
+    stats[0] = steps;
+    stats[1] = accepted;
+    stats[2] = proposed;
+  }
+  return SV_OK;
+}
+
 int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head) {
   if (!ctx || K < 1) return SV_E_INVAL;
   return 1 + 6 * ctx->cfg.n_layers + (with_head ? 2 : 1);

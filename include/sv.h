@@ -133,6 +133,30 @@ int sv_sync(sv_ctx* ctx);
  * positions and release their pages.  Synchronous. */
 int sv_truncate(sv_ctx* ctx, int new_len);
 
+/* Greedy speculative generation: `draft` proposes, `target` verifies.
+ * (Phase 23: Speculative Verify Parity, section 2: drafts are checked by one
+ * batched target forward, the longest matching prefix is accepted and the
+ * rejected tail rolled back.)  Both contexts hold the same committed tokens
+ * (e.g. one prompt prefilled into each) and share the vocabulary; `pending`
+ * is the target's greedy token after them (sv_prefill's next_token).  Each
+ * round the drafter decodes K-1 tokens after the pending one, the target
+ * verifies the K-row block [pending, drafts], and the drafter is rolled back
+ * (or advanced) to the target's length.  Rounds run until at least n_new
+ * tokens are committed.  The tokens are the target's own greedy continuation,
+ * whatever the drafter proposes.
+ *   K in [1, target max_k]; K = 1 is plain decoding.  Both contexts need
+ *   max_seq >= length + n_new + K.
+ *   out_tokens: host int32 [n_new + K - 1]; *n_out (n_new .. n_new + K - 1)
+ *   of them are written: every token committed, in order, starting with
+ *   `pending`.  *next_pending: the target's greedy token after them.
+ *   stats (or NULL): int32 [3] = {verify steps, drafts accepted, drafts
+ *   proposed}.
+ * Errors: SV_E_INVAL (arguments), SV_E_STATE (lengths differ or asynchronous
+ * work pending), or those of the calls it makes (a drafter's error is
+ * reported through the target's sv_last_error).  Synchronous. */
+int sv_spec_generate(sv_ctx* target, sv_ctx* draft, int32_t pending, int K, int n_new,
+                     int32_t* out_tokens, int32_t* n_out, int32_t* next_pending, int32_t* stats);
+
 /* Current committed length (as of the last synchronous call or sv_sync). */
 int sv_seq_len(const sv_ctx* ctx);
 

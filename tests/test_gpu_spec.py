@@ -1,0 +1,107 @@
+"""The draft -> verify loop (sv_spec_generate) end to end on the GPU: what it
+commits is the target's own greedy continuation whatever the drafter proposes
+("Phase 23: Speculative Verify Parity", sections 1-2: verify must commit
+exactly what single-token decoding would)."""
+import pytest
+
+import inputs
+from tests import gpu_helpers as gh
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+def _greedy(cfg, dw, prompt, n, max_seq):
+    ctx = gh.context(cfg, dw, max_k=8, max_seq=max_seq)
+    chain = [ctx.prefill(prompt)]
+    while len(chain) < n:
+        chain.append(ctx.decode(chain[-1]))
+    ctx.close()
+    return chain
+
+
+def _pair(tcfg, tw, dcfg, dw, prompt, max_seq, shuffle=None):
+    tgt = gh.context(tcfg, tw, max_k=8, max_seq=max_seq)
+    drf = gh.context(dcfg, dw, max_k=8, max_seq=max_seq, shuffle=shuffle)
+    pending = tgt.prefill(prompt)
+    drf.prefill(prompt)
+    return tgt, drf, pending
+
+
+@pytest.mark.parametrize("K", [1, 2, 4, 8])
+def test_self_draft_accepts_everything(K):
+    """A drafter with the target's own weights proposes exactly the target's
+    greedy tokens (decode rows are bit-identical to verify rows), so every
+    draft is accepted and each verify step commits K tokens."""
+    import greedy_speculative_decode_gb300 as sv
+    cfg = inputs.TINY
+    _, dw = gh.make(cfg, seed=0, gain_std=0.1, host=False)
+    prompt = inputs.prefix_tokens(80, 21, cfg.vocab)
+    n = 40
+    ref = _greedy(cfg, dw, prompt, n + K, 128)
+    tgt, drf, pending = _pair(cfg, dw, cfg, dw, prompt, 128, shuffle=3)
+    toks, nxt, st = sv.spec_generate(tgt, drf, pending, K, n)
+    steps = -(-n // K)
+    assert toks == ref[:steps * K] and nxt == ref[steps * K]
+    assert st["verify_steps"] == steps
+    assert st["accepted"] == st["proposed"] == steps * (K - 1)
+    assert len(tgt) == len(drf) == len(prompt) + steps * K
+
+
+@pytest.mark.parametrize("K", [2, 4, 8])
+def test_other_drafter_still_gives_greedy_output(K):
+    """A drafter with unrelated weights is mostly rejected; the tokens are the
+    target's greedy chain all the same, and the drafter is kept in step (a
+    second call continues where the first stopped)."""
+    import greedy_speculative_decode_gb300 as sv
+    cfg = inputs.TINY
+    _, dw = gh.make(cfg, seed=0, gain_std=0.1, host=False)
+    _, dw2 = gh.make(cfg, seed=7, gain_std=0.1, host=False)
+    prompt = inputs.prefix_tokens(81, 17, cfg.vocab)
+    ref = _greedy(cfg, dw, prompt, 80, 160)
+    tgt, drf, pending = _pair(cfg, dw, cfg, dw2, prompt, 160)
+    toks, nxt, st = sv.spec_generate(tgt, drf, pending, K, 33)
+    assert 33 <= len(toks) <= 33 + K - 1
+    assert toks == ref[:len(toks)] and nxt == ref[len(toks)]
+    assert 0 <= st["accepted"] <= st["proposed"] == st["verify_steps"] * (K - 1)
+    assert len(drf) == len(tgt) == len(prompt) + len(toks)
+    more, nxt2, _ = sv.spec_generate(tgt, drf, nxt, K, 20)
+    assert toks + more == ref[:len(toks) + len(more)] and nxt2 == ref[len(toks) + len(more)]
+
+
+def test_small_drafter_for_8b_shaped_target():
+    """An 8B-shaped target (one layer, full width and vocabulary) with a
+    0.6B-shaped drafter (two layers) on the same kernels."""
+    import greedy_speculative_decode_gb300 as sv
+    tcfg = inputs.shrink(inputs.QWEN3_8B, n_layers=1)
+    dcfg = inputs.shrink(inputs.QWEN3_0P6B, n_layers=2)
+    _, tw = gh.make(tcfg, seed=0, gain_std=0.1, host=False)
+    _, dw = gh.make(dcfg, seed=1, gain_std=0.1, host=False)
+    prompt = inputs.prefix_tokens(82, 40, tcfg.vocab)
+    ref = _greedy(tcfg, tw, prompt, 30, 96)
+    tgt, drf, pending = _pair(tcfg, tw, dcfg, dw, prompt, 96)
+    toks, nxt, st = sv.spec_generate(tgt, drf, pending, 4, 20)
+    assert toks == ref[:len(toks)] and nxt == ref[len(toks)]
+    assert st["proposed"] == 3 * st["verify_steps"]
+
+
+def test_bad_calls_are_rejected():
+    import greedy_speculative_decode_gb300 as sv
+    cfg = inputs.TINY
+    _, dw = gh.make(cfg, seed=0, gain_std=0.1, host=False)
+    tgt, drf, pending = _pair(cfg, dw, cfg, dw, [1, 2, 3], 64)
+    for K, n in ((0, 5), (9, 5), (2, 0), (4, 60)):  # max_k is 8, max_seq 64
+        with pytest.raises(sv.SvError) as e:
+            sv.spec_generate(tgt, drf, pending, K, n)
+        assert e.value.code == sv.SV_E_INVAL, (K, n)
+    for bad in (-1, cfg.vocab):
+        with pytest.raises(sv.SvError) as e:
+            sv.spec_generate(tgt, drf, bad, 2, 5)
+        assert e.value.code == sv.SV_E_INVAL
+    with pytest.raises(sv.SvError) as e:
+        sv.spec_generate(tgt, tgt, pending, 2, 5)
+    assert e.value.code == sv.SV_E_INVAL
+    tgt.prefill([4])
+    with pytest.raises(sv.SvError) as e:  # lengths differ
+        sv.spec_generate(tgt, drf, pending, 2, 5)
+    assert e.value.code == sv.SV_E_STATE
