@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--vocab", type=int, default=None, help="override the vocabulary size")
     ap.add_argument("--spec", action="store_true",
                     help="time the draft -> verify loop against plain decoding (separate JSON line)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time sv_prefill of --prefix tokens (separate JSON line)")
     ap.add_argument("--linear-only", action="store_true",
                     help="time each linear class once per layer (NVTX range 'linear') and exit")
     return ap.parse_args()
@@ -402,6 +404,38 @@ def run_spec(args):
     print(json.dumps(out))
 
 
+def run_prefill(args):
+    """Prompt prefill throughput: sv_prefill of --prefix tokens on a context of
+    max_k = --K, wall clock around the synchronous call (best of 3 after a
+    warm-up), and the weight stream it implies (every weight once per row
+    block) against the measured HBM peak."""
+    import torch
+
+    import greedy_speculative_decode_gb300 as sv
+    cfg = model_config(args)
+    hbm_peak, _ = peaks()
+    w = inputs.device_weights(cfg, seed=0, gain_std=0.0)
+    n = args.prefix
+    ctx = sv.Context(cfg, w, max_k=args.K, max_seq=n + 8)
+    prompt = inputs.prefix_tokens(0, n, cfg.vocab)
+    best = None
+    for r in range(4):
+        ctx.truncate(0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ctx.prefill(prompt)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if r > 0:
+            best = dt if best is None else min(best, dt)
+    blocks = math.ceil(n / sv.MAX_K)
+    streamed = blocks * cfg.weight_bytes() + n * cfg.kv_bytes_per_token()
+    print(json.dumps({"mode": "prefill", "config": cfg.name, "tokens": n, "max_k": args.K,
+                      "row_block": sv.MAX_K, "seconds": best, "tok_s": n / best,
+                      "weight_passes": blocks, "streamed_GB": streamed / 1e9,
+                      "hbm_frac": streamed / best / 1e9 / hbm_peak}))
+
+
 def run_ours(args):
     import torch
 
@@ -410,6 +444,8 @@ def run_ours(args):
         return run_linear_only(args)
     if args.spec:
         return run_spec(args)
+    if args.prefill:
+        return run_prefill(args)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -492,7 +492,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
     return bail(rc);
 
   // ---- device memory
-  const int MP = mp_of(c.max_k);
+  const int MP = mp_of(kMaxK);  // prefill blocks take kMaxK rows whatever max_k is
   ctx->bt_len = pages_for(c.max_seq);
   ctx->layer_stride = (size_t)c.max_pages * Hkv * kPage * d;
   const size_t pool = ctx->layer_stride * (L > 0 ? L : 1);
@@ -516,8 +516,8 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->a, (size_t)kMaxK * c.ffn)) ||
       (rc = dalloc(ctx, &ctx->x_ss, (size_t)kMaxK * (H / 128))) ||
       (rc = dalloc(ctx, &ctx->rope, (size_t)c.max_seq * (d / 2))) ||
-      (rc = dalloc(ctx, &ctx->part_ml, (size_t)c.max_k * Hq * ctx->max_splits)) ||
-      (rc = dalloc(ctx, &ctx->part_o, (size_t)c.max_k * Hq * ctx->max_splits * d)) ||
+      (rc = dalloc(ctx, &ctx->part_ml, (size_t)kMaxK * Hq * ctx->max_splits)) ||
+      (rc = dalloc(ctx, &ctx->part_o, (size_t)kMaxK * Hq * ctx->max_splits * d)) ||
       (rc = dalloc(ctx, &ctx->ws, ws_words)) ||
       (rc = dalloc(ctx, &ctx->am_val, (size_t)kMaxK * ctx->lin_head.n_tiles)) ||
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
@@ -526,7 +526,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage))
     return bail(SV_E_CUDA);
   // a prefill of max_seq tokens stages every block [cap_len, tokens] side by side
-  ctx->pin_in_len = (size_t)c.max_seq + (c.max_seq + c.max_k - 1) / c.max_k + kMaxK + 8;
+  ctx->pin_in_len = (size_t)c.max_seq + (c.max_seq + kMaxK - 1) / kMaxK + kMaxK + 8;
   if (cudaMallocHost(&ctx->pin_in, sizeof(int32_t) * ctx->pin_in_len) != cudaSuccess ||
       cudaMallocHost(&ctx->pin_out, sizeof(int32_t) * 8) != cudaSuccess ||
       cudaMallocHost(&ctx->pin_bt, sizeof(int) * (size_t)ctx->bt_len) != cudaSuccess)
@@ -590,7 +590,9 @@ int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logit
     return fail(ctx, SV_E_INVAL, "length %d + %d exceeds max_seq", ctx->seq_len, n);
   if ((rc = begin_call(ctx))) return rc;
   if ((rc = ensure_pages(ctx, ctx->seq_len + n))) return rc;
-  const int B = ctx->cfg.max_k;
+  // blocks of as many rows as a step holds, whatever max_k: each block streams
+  // every weight once, and no row's arithmetic depends on the block's size
+  const int B = kMaxK;
   int at = 0;
   for (int done = 0; done < n; done += B) {
     const int M = std::min(B, n - done);

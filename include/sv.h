@@ -94,7 +94,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
 void sv_destroy(sv_ctx* ctx);
 
 /* Commit n tokens (host array) at positions len .. len+n-1, processed in
- * row blocks of at most max_k rows.  last_logits_dev: device fp32 [vocab] for
+ * row blocks of up to 32 rows (whatever max_k is).  last_logits_dev: device fp32 [vocab] for
  * the logits after the last token, or NULL.  next_token: the greedy token
  * after the last one.  Synchronous. */
 int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logits_dev,
