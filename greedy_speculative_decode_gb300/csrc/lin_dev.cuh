@@ -624,6 +624,8 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
   const int a_khalf = lane >> 4;
   const uint32_t xs_base =
       smem_u32(sm.xs) + (uint32_t)(((lane & 7) * XS + ((lane >> 3) & 1) * 8) * sizeof(bf16));
+  // x4 form: lanes 16-31 address token rows 8-15 (the next token tile)
+  const uint32_t xs_base4 = xs_base + (uint32_t)(((lane >> 4) & 1) * 8 * XS * sizeof(bf16));
   float acc[MT][4];
 #pragma unroll
   for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
@@ -691,19 +693,30 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
       const int s = it & (kLinStages - 1);
       if (ok && !mbar_wait(&sm.full[s], (uint32_t)(it / kLinStages) & 1u)) ok = false;
       if (ok) {
+        // every fragment of the block first, then the mma: the loads are
+        // issued back to back instead of each waiting behind the previous mma
+        // (each accumulator still takes its k16 steps in order)
         const uint32_t tile_base = smem_u32(sm.ring + s * kLinStageBytes + chunk * kLinChunkBytes);
+        constexpr int K16 = kLinBK / 16;
+        uint32_t a[K16][4], b[K16][MT][2];
 #pragma unroll
-        for (int k16 = 0; k16 < kLinBK / 16; ++k16) {
-          uint32_t a[4];
+        for (int k16 = 0; k16 < K16; ++k16) {
           const int kc = k16 * 2 + a_khalf;
-          ldsm_x4(tile_base + a_row * 128 + ((kc ^ (a_row & 7)) << 4), a[0], a[1], a[2], a[3]);
+          ldsm_x4(tile_base + a_row * 128 + ((kc ^ (a_row & 7)) << 4), a[k16][0], a[k16][1], a[k16][2],
+                  a[k16][3]);
+          if (MT == 1) {
+            ldsm_x2(xs_base + (uint32_t)((xcol + k16 * 16) * sizeof(bf16)), b[k16][0][0], b[k16][0][1]);
+          } else {
 #pragma unroll
-          for (int t = 0; t < MT; ++t) {
-            uint32_t b0, b1;
-            ldsm_x2(xs_base + (uint32_t)(((t * 8) * XS + xcol + k16 * 16) * sizeof(bf16)), b0, b1);
-            mma_bf16(acc[t], a, b0, b1);
+            for (int t = 0; t < MT; t += 2)  // the fragments of token tiles t and t + 1 at once
+              ldsm_x4(xs_base4 + (uint32_t)(((t * 8) * XS + xcol + k16 * 16) * sizeof(bf16)), b[k16][t][0],
+                      b[k16][t][1], b[k16][t + 1 < MT ? t + 1 : t][0], b[k16][t + 1 < MT ? t + 1 : t][1]);
           }
         }
+#pragma unroll
+        for (int k16 = 0; k16 < K16; ++k16)
+#pragma unroll
+          for (int t = 0; t < MT; ++t) mma_bf16(acc[t], a[k16], b[k16][t][0], b[k16][t][1]);
       }
       fence_proxy_async_smem();  // our ldmatrix reads of stage s precede its next TMA write
       __syncwarp();
