@@ -193,3 +193,31 @@ def test_long_context_forced_patterns(qwen8b, plen):
         kv, vv = ver.kv_read(layer, plen - 16, i + 16)
         assert torch.equal(kd.view(torch.int16), kv.view(torch.int16))
         assert torch.equal(vd.view(torch.int16), vv.view(torch.int16))
+
+
+def test_gemma_like_long_context_crosses_attention_forms(gemma):
+    """head_dim 256 at a 4100-id prefix (17 attention splits): a 32-row
+    verify runs the attention form whose CTAs take several items and the
+    long split merge, single-token decode the one-item form; every accepted
+    row equals decode bit for bit, and so does the committed K/V."""
+    cfg, hw, dw = gemma
+    plen = 4100
+    prompt = inputs.prefix_tokens(61, plen, cfg.vocab)
+    dec = gh.context(cfg, dw, max_k=32, max_seq=plen + 80)
+    chain, rows = _decode_rows(dec, dec.prefill(prompt), 50, cfg.vocab)
+    ver = gh.context(cfg, dw, max_k=32, max_seq=plen + 80, shuffle=11)
+    ver.prefill(prompt)
+    for K, reject_at in ((32, None), (16, 5)):
+        i = len(ver) - plen
+        toks, n_exp = inputs.window(chain, i, K, vocab=cfg.vocab, reject_at=reject_at)
+        lg = gh.logits_buf(K, cfg.vocab)
+        n, corr = ver.verify(toks, logits=lg)
+        assert n == n_exp and corr == chain[i + n + 1], (K, n, n_exp)
+        for r in range(n + 1):
+            assert torch.equal(lg[r], rows[i + r][0]), (K, r)
+    m = len(ver) - plen
+    for layer in range(cfg.n_layers):
+        kd, vd = dec.kv_read(layer, plen - 8, m + 8)
+        kv, vv = ver.kv_read(layer, plen - 8, m + 8)
+        assert torch.equal(kd.view(torch.int16), kv.view(torch.int16))
+        assert torch.equal(vd.view(torch.int16), vv.view(torch.int16))
