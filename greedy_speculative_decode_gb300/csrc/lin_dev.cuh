@@ -81,7 +81,8 @@ __device__ __forceinline__ float act_fn(float g, int act) {
 template <int MP>
 struct EpiPre {
   static constexpr int N = (kLinRows * MP + kLinConsumerWarps * 32 - 1) / (kLinConsumerWarps * 32);
-  float res[N];   // EPI_RESID: the residual x[m, n0 + lr]
+  float res[N];   // EPI_RESID: the residual x[m, n0 + lr]; QKV, head_dim 128: the
+                  // QK-norm gain of elements lane + 32 j (j < 4)
   float2 cs[N];   // EPI_QKV: (cos, sin) of the element's RoPE angle
   int page[N];    // EPI_QKV: physical page of position pos + m (-1: none)
 };
@@ -106,6 +107,11 @@ __device__ __forceinline__ void epi_preload(const LinParams& p, int tile, int po
     // m = warp + 8 k, lane's RoPE angles for elements lane and lane + 32
     const int warp = tid >> 5, lane = tid & 31, half = kLinRows / 2;
     const bool kv = tile * kLinRows >= p.n_q_heads * kLinRows;
+    if (p.q_gain != nullptr && tile < p.n_q_heads + p.n_kv_heads) {  // q or k: its norm gain
+      const bf16* g = kv ? p.k_gain : p.q_gain;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) pre.res[j] = __bfloat162float(g[lane + 32 * j]);
+    }
 #pragma unroll
     for (int k = 0; k < MP / 8; ++k) {
       const int m = warp + 8 * k;
@@ -167,10 +173,8 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
         for (int j = 0; j < 4; ++j) ss = __fadd_rn(ss, __fmul_rn(v[j], v[j]));
         for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
         const float r = 1.0f / sqrtf(ss / (float)d + p.eps);
-        const bf16* g = is_q ? p.q_gain : p.k_gain;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          v[j] = bf16r(__fmul_rn(bf16r(__fmul_rn(v[j], r)), __bfloat162float(g[lane + 32 * j])));
+        for (int j = 0; j < 4; ++j) v[j] = bf16r(__fmul_rn(bf16r(__fmul_rn(v[j], r)), pre.res[j]));
       }
       float outv[4] = {v[0], v[1], v[2], v[3]};
       if (is_q || is_k) {

@@ -235,3 +235,24 @@ def test_decode_past_split_boundaries_bitexact(tiny):
     assert n == 11
     for r in range(12):
         assert torch.equal(lg[r], rows[r][0]), r
+
+
+def test_prefill_blocks_do_not_depend_on_max_k(tiny):
+    """Prefill runs 32-row blocks whatever max_k is: a 100-token prompt
+    committed by contexts with max_k 1, 4 and 32 gives the same next token
+    and the same K/V as committing it one decode at a time."""
+    cfg, hw, dw = tiny
+    prompt = inputs.prefix_tokens(77, 100, cfg.vocab)
+    ref = gh.context(cfg, dw, max_k=1, max_seq=128)
+    ref.prefill(prompt[:1])
+    for t in prompt[1:-1]:
+        ref.decode(t)
+    nxt = ref.decode(prompt[-1])
+    for mk in (1, 4, 32):
+        ctx = gh.context(cfg, dw, max_k=mk, max_seq=128, shuffle=mk)
+        assert ctx.prefill(prompt) == nxt, mk
+        for layer in range(cfg.n_layers):
+            ka, va = ref.kv_read(layer, 0, 100)
+            kb, vb = ctx.kv_read(layer, 0, 100)
+            assert torch.equal(ka.view(torch.int16), kb.view(torch.int16)), (mk, layer)
+            assert torch.equal(va.view(torch.int16), vb.view(torch.int16)), (mk, layer)
