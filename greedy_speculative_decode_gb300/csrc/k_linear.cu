@@ -129,7 +129,7 @@ size_t linear_smem_bytes(int mt) {
   b += (size_t)kLinStages * kLinStageBytes;
   b += (size_t)mp * (xc + 8) * sizeof(bf16);
   b += ((size_t)kLinRows * (mp + 1) * sizeof(float) + 15) & ~size_t(15);
-  b += (size_t)xc * sizeof(bf16);  // gain window
+  b += (size_t)kLinXCols * sizeof(bf16);  // gain window
   b += (2 * kLinStages + 2) * sizeof(uint64_t) + (kMaxK + 64) * sizeof(float) + 16;
   return b;
 }

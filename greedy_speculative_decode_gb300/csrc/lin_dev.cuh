@@ -471,7 +471,7 @@ __device__ __forceinline__ LinSmem lin_smem(uint8_t* smem) {
   sm.T = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sm.xs) + MP * XS * sizeof(bf16));
   sm.gs = reinterpret_cast<bf16*>(reinterpret_cast<uint8_t*>(sm.T) +
                                   ((kLinRows * TS * sizeof(float) + 15) & ~size_t(15)));
-  sm.full = reinterpret_cast<uint64_t*>(sm.gs + XC);
+  sm.full = reinterpret_cast<uint64_t*>(sm.gs + kLinXCols);  // the gain of windows up to 4096 columns
   sm.empty = sm.full + kLinStages;
   sm.xbar = sm.empty + kLinStages;
   sm.gbar = sm.xbar + 1;
@@ -587,7 +587,10 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
   const int ngroups = (ncols + kGroup - 1) / kGroup;
 
   // ---- before the wait on the previous kernel: nothing here depends on it
-  if (NORM && one_chunk && tid == 0) {  // the gain window
+  // the gain window, staged whole for windows of up to kLinXCols columns
+  // (a window of several chunks then normalises each chunk from it)
+  const bool gain_staged = NORM && ncols <= kLinXCols;
+  if (gain_staged && tid == 0) {
     const int first = min(ncols, p.Kd - c0);
     mbar_arrive_expect_tx(sm.gbar, (uint32_t)(ncols * sizeof(bf16)));
     bulk_load(sm.gs, p.gain + c0, (uint32_t)(first * sizeof(bf16)), sm.gbar);
@@ -680,10 +683,12 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
           if (!mbar_wait(sm.xbar, xphase)) ok = false;
           xphase ^= 1u;
           if (NORM) {
+            if (gain_staged && staged < 0 && !mbar_wait(sm.gbar, 0)) ok = false;
             for (int c8 = tid; c8 * 8 < nc; c8 += nthr) {
               int k = c0 + t0 + c8 * 8;
               if (k >= Kd) k -= Kd;
-              const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.gain + k));
+              const uint4 gv = gain_staged ? reinterpret_cast<const uint4*>(sm.gs)[t0 / 8 + c8]
+                                           : __ldg(reinterpret_cast<const uint4*>(p.gain + k));
               for (int m = 0; m < p.M; ++m) {
                 uint4* ptr = reinterpret_cast<uint4*>(sm.xs + (size_t)m * XS + c8 * 8);
                 *ptr = norm8(*ptr, sm.s_rstd[m], gv);
