@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kLinThreads, 1)
   if (warp == kLinConsumerWarps) {  // producer: weights do not depend on earlier kernels
     if (lane == 0) {
       prefetch_tensormap(&wmap);
-      if (!lin_produce(p, &wmap, blockIdx.x, gridDim.x, sm, it, policy_evict_first()))
+      if (!lin_produce<LinGeom<MT>::kStages>(p, &wmap, blockIdx.x, gridDim.x, sm, it, policy_evict_first()))
         atomicOr(&p.st->status, ST_TIMEOUT);
       else
         lin_prefetch_next(p, &pfmap, blockIdx.x);
@@ -124,9 +124,10 @@ cudaError_t launch_mt(const LinearDesc& d, const LinParams& p, int epi, bool nor
 
 size_t linear_smem_bytes(int mt) {
   const int mp = mt * 8;
-  const int xc = kLinXCols / mt;
+  const int xc = mt == 2 ? LinGeom<2>::kXCols : (mt == 4 ? LinGeom<4>::kXCols : LinGeom<1>::kXCols);
+  const int stages = mt == 2 ? LinGeom<2>::kStages : (mt == 4 ? LinGeom<4>::kStages : LinGeom<1>::kStages);
   size_t b = 1024;  // alignment slack
-  b += (size_t)kLinStages * kLinStageBytes;
+  b += (size_t)stages * kLinStageBytes;
   b += (size_t)mp * (xc + 8) * sizeof(bf16);
   b += ((size_t)kLinRows * (mp + 1) * sizeof(float) + 15) & ~size_t(15);
   b += (size_t)kLinXCols * sizeof(bf16);  // gain window

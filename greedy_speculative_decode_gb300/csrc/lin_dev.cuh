@@ -464,10 +464,10 @@ struct LinSmem {
 
 template <int MT>
 __device__ __forceinline__ LinSmem lin_smem(uint8_t* smem) {
-  constexpr int MP = MT * 8, TS = MP + 1, XC = kLinXCols / MT, XS = XC + 8;
+  constexpr int MP = MT * 8, TS = MP + 1, XC = LinGeom<MT>::kXCols, XS = XC + 8;
   LinSmem sm;
   sm.ring = smem;
-  sm.xs = reinterpret_cast<bf16*>(smem + kLinStages * kLinStageBytes);
+  sm.xs = reinterpret_cast<bf16*>(smem + LinGeom<MT>::kStages * kLinStageBytes);
   sm.T = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sm.xs) + MP * XS * sizeof(bf16));
   sm.gs = reinterpret_cast<bf16*>(reinterpret_cast<uint8_t*>(sm.T) +
                                   ((kLinRows * TS * sizeof(float) + 15) & ~size_t(15)));
@@ -493,6 +493,7 @@ __device__ __forceinline__ void lin_range(const LinParams& p, int cta, int G, lo
 // Producer (one thread): TMA the CTA's weight boxes into the ring.  `it`
 // counts ring uses (stage = it mod stages, parity = its quotient's low bit),
 // kept in step with the consumers'.  Returns false on a timeout.
+template <int S>  // ring stages
 __device__ bool lin_produce(const LinParams& p, const CUtensorMap* wmap, int cta, int G,
                             const LinSmem& sm, int& it, uint64_t pol) {
   const int KB = p.Kd / kLinBK;
@@ -500,8 +501,8 @@ __device__ bool lin_produce(const LinParams& p, const CUtensorMap* wmap, int cta
   lin_range(p, cta, G, kb_begin, kb_end);
   int tile = (int)(kb_begin / KB), kk = (int)(kb_begin % KB);  // walked without division
   for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
-    const int s = it % kLinStages;
-    if (it >= kLinStages && !mbar_wait(&sm.empty[s], ((it / kLinStages) & 1) ^ 1)) return false;
+    const int s = it % S;
+    if (it >= S && !mbar_wait(&sm.empty[s], ((it / S) & 1) ^ 1)) return false;
     const TileRows tr = tile_rows(p, tile);
     mbar_arrive_expect_tx(&sm.full[s], kLinStageBytes);
     uint8_t* dst = sm.ring + s * kLinStageBytes;
@@ -566,7 +567,8 @@ template <int MT, int EPI, bool NORM>
 __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& sm, int& it) {
   constexpr int MP = MT * 8;          // padded token rows
   constexpr int TS = MP + 1;          // epilogue tile row stride
-  constexpr int XC = kLinXCols / MT;  // input columns staged at once
+  constexpr int XC = LinGeom<MT>::kXCols;  // input columns staged at once
+  constexpr int S = LinGeom<MT>::kStages;  // ring stages
   constexpr int XS = XC + 8;          // staged row stride in elements (16B pad: no bank conflicts)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nthr = kLinConsumerWarps * 32;
@@ -638,7 +640,7 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
   for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
   EpiPre<MP> pre;
 
-  static_assert((kLinStages & (kLinStages - 1)) == 0, "the ring index is taken with a mask");
+  static_assert((S & (S - 1)) == 0, "the ring index is taken with a mask");
   const int Kd = p.Kd;
   int staged = one_chunk ? 0 : -1;  // chunk in xs
   uint32_t xphase = 0;
@@ -699,8 +701,8 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
           staged = xchunk;
         }
       }
-      const int s = it & (kLinStages - 1);
-      if (ok && !mbar_wait(&sm.full[s], (uint32_t)(it / kLinStages) & 1u)) ok = false;
+      const int s = it & (S - 1);
+      if (ok && !mbar_wait(&sm.full[s], (uint32_t)(it / S) & 1u)) ok = false;
       if (ok) {
         // every fragment of the block first, then the mma: the loads are
         // issued back to back instead of each waiting behind the previous mma

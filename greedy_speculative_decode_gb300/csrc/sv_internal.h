@@ -22,8 +22,16 @@ constexpr int kLinChunkBytes = 64 * 128;           // one 64 x 64 bf16 box, 128B
 constexpr int kLinStageBytes = 2 * kLinChunkBytes;  // both chunks of one k block
 constexpr int kLinStages = 8;
 // Input columns a CTA stages at once, for 8 padded token rows (half as many
-// for 16, a quarter for 32): 64 KB of shared memory.
+// for 16): 64 KB of shared memory.
 constexpr int kLinXCols = 4096;
+// Ring stages and staged input columns of the kernel for MT tiles of 8 token
+// rows.  32 rows (MT = 4) give up half the ring for a 2048-column window:
+// half as many restages of 4096-wide inputs, on steps the ring does not bound.
+template <int MT>
+struct LinGeom {
+  static constexpr int kStages = MT == 4 ? kLinStages / 2 : kLinStages;
+  static constexpr int kXCols = MT == 4 ? kLinXCols / 2 : kLinXCols / MT;
+};
 // Fewest k-blocks (16 KB of weight each) a CTA streams: small matrices use
 // fewer CTAs rather than split tiles into many tiny partial sums.
 constexpr int kLinMinShare = 4;
