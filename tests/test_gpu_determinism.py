@@ -58,3 +58,46 @@ def test_independent_contexts_identical(wide):
         for (k, v), (k0, v0) in zip(kv, outs[0][1]):
             assert torch.equal(k.view(torch.int16), k0.view(torch.int16))
             assert torch.equal(v.view(torch.int16), v0.view(torch.int16))
+
+
+def test_concurrent_contexts_share_the_gpu(wide):
+    """Two contexts on their own streams, their asynchronous verify steps
+    issued back to back with no sync in between, so their grids share the
+    SMs.  Every result and every logit equals the same windows run one
+    context at a time; no kernel reports a timeout (the split-tile exchange
+    waits only on CTAs dispatched before it)."""
+    cfg, dw = wide
+    prompts = [inputs.prefix_tokens(90 + i, 300 + 37 * i, cfg.vocab) for i in range(2)]
+    wins = [[[5 + j, 9, 13, 21][:4] for j in range(6)] for _ in range(2)]
+
+    def run(concurrent):
+        ctxs = [gh.context(cfg, dw, max_k=8, max_seq=400, shuffle=i) for i in range(2)]
+        res, lgs = [], []
+        for i, c in enumerate(ctxs):
+            t = c.prefill(prompts[i])
+            for w in wins[i]:
+                w[0] = t  # any committed token works; fix the same one for both runs
+            c.reserve(len(c) + 6 * 4)
+        bufs = [[torch.zeros(4, dtype=torch.int32, device="cuda") for _ in range(6)] for _ in range(2)]
+        logit = [[gh.logits_buf(4, cfg.vocab) for _ in range(6)] for _ in range(2)]
+        toks = [[torch.tensor(w, dtype=torch.int32, device="cuda") for w in wins[i]] for i in range(2)]
+        for s in range(6):
+            for i in (0, 1):
+                ctxs[i].verify_async(toks[i][s], 4, bufs[i][s], logit[i][s])
+                if not concurrent:
+                    ctxs[i].sync()
+        for c in ctxs:
+            c.sync()
+        torch.cuda.synchronize()
+        out = [[b.cpu().tolist() for b in bufs[i]] for i in range(2)]
+        for c in ctxs:
+            c.close()
+        return out, logit
+
+    seq, lseq = run(False)
+    con, lcon = run(True)
+    assert seq == con
+    assert all(r[3] == 0 for i in range(2) for r in con[i])
+    for i in range(2):
+        for s in range(6):
+            assert torch.equal(lseq[i][s], lcon[i][s]), (i, s)
