@@ -54,6 +54,13 @@ def test_no_alloc_lm_head_matches_context_wide():
     _compare(cfg, [11, 2049, 30000, 7], seed=4)
 
 
+def test_no_alloc_lm_head_matches_context_32_rows():
+    """32 rows: the four-token-tile kernel with its own ring and window
+    geometry, against the context's LM head on the same rows."""
+    cfg = inputs.shrink(inputs.QWEN3_8B, n_layers=0, vocab=32768)
+    _compare(cfg, [(7919 * j + 11) % 32768 for j in range(32)], seed=5)
+
+
 def test_no_alloc_lm_head_matches_context_full_vocab():
     """The 151,936-id vocabulary of the 8B-shaped model (1187 tiles, split
     tiles between neighbouring CTAs) fits the fixed scratch."""
