@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsv.so")
-SOURCES = ["k_linear.cu", "k_attn.cu", "k_misc.cu", "sv_api.cu", "sv_noalloc.cu"]
+SOURCES = ["k_linear.cu", "k_linear_tc.cu", "k_attn.cu", "k_misc.cu", "sv_api.cu", "sv_noalloc.cu"]
 
 # --fmad=false: every fused multiply-add in the kernels is written out, so
 # the rounding of each element never depends on what the compiler contracts.

@@ -1,0 +1,561 @@
+// k_linear_tc.cu -- the batch-invariant linear for blocks of 17 to 32 rows on
+// the fifth-generation tensor cores (tcgen05): Y[m, n] = sum_k X[m, k] W[n, k].
+//
+// Same weight stream, split and epilogues as the mma.sync form, with the
+// multiply moved off the consumer warps.  Each ring stage holds a 128-row x
+// 64-column weight block (two TMA boxes) and the 32 x 64 block of the input
+// rows at the same columns (one TMA box; rows past M are never stored).  One
+// thread issues, per block, four tcgen05.mma of 128 x 32 x 16 (weight rows
+// as the 128-row operand, token rows as the 32-column one) into an fp32
+// accumulator in tensor memory; a tile piece (a CTA's run of k-blocks inside
+// one 128-row tile) starts from zero, two accumulators alternate so the next
+// piece runs while the consumers read the last one back.
+//
+// Bit-identity with the mma.sync form (and so with single-token decode):
+// every output element is the fp32 sum of the same products taken 16 k at a
+// time in k order from zero, which the two instructions round identically
+// (checked element by element on random, small-weight and wide-range
+// operands); pieces and split partials are summed in the same order.
+//
+// Roles: warps 0-7 consumers (RMSNorm of each stage's input rows in place
+// when the linear has a norm prologue, accumulator read-back, split-tile
+// exchange, epilogues), warp 8 the TMA producer, warp 9 the MMA issuer.
+// Every wait is bounded; on a timeout the kernel raises ST_TIMEOUT, waits
+// (bounded) for its own copies and multiplies, and frees its tensor memory.
+#include "lin_dev.cuh"
+#include "linear_tc.h"
+
+namespace sv {
+namespace {
+
+constexpr int kTcStages = 8;
+constexpr int kTcMP = 32;                                  // padded token rows
+constexpr int kTcXBytes = kTcMP * 128;                     // 32 rows x 64 columns, 128B-swizzled
+constexpr int kTcStageBytes = kLinStageBytes + kTcXBytes;  // 20 KB, a multiple of 1024
+constexpr int kTcThreads = (kLinConsumerWarps + 2) * 32;
+constexpr int kTcProducerWarp = kLinConsumerWarps, kTcMmaWarp = kLinConsumerWarps + 1;
+constexpr int kTcCols = 2 * kTcMP;                         // tensor-memory columns: two accumulators
+static_assert(kTcStageBytes % 1024 == 0, "swizzle atoms stay aligned");
+
+// ---------------------------------------------------------------- tcgen05
+// Shared-memory operand descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the TMA box layout); start address >> 4 in bits 0-13,
+// leading offset 1 (unused by swizzled K-major operands), stride 1024 >> 4 in
+// bits 32-45, descriptor version 1 at bit 46, layout 2 (128B swizzle) at 61.
+__device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major; N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accum)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Eight consecutive accumulator columns of the warp's 32 lanes.
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- layout
+struct TcSmem {
+  uint8_t* ring;        // [kTcStages][W 16 KB | X 4 KB]
+  float* T;             // [128][kTcMP + 1] epilogue tile
+  uint64_t* full;       // [S] the stage's weight and input bytes landed
+  uint64_t* xnorm;      // [S] the stage's input rows are normalised (by one consumer warp)
+  uint64_t* empty;      // [S] the multiplies reading the stage completed
+  uint64_t* acc_full;   // [2] an accumulator holds a finished piece
+  uint64_t* acc_empty;  // [2] the consumers read it back (8 consumer warps)
+  uint64_t* drain;      // the issuer's last multiplies completed
+  uint64_t* gbar;       // the gain window landed
+  bf16* gs;             // [kLinXCols] gain of the CTA's input window (norm prologue)
+  float* s_rstd;        // [kMaxK]
+  float* s_hrstd;       // [64]
+  uint32_t* taddr;      // tensor-memory base address from tcgen05.alloc
+};
+
+__device__ __forceinline__ TcSmem tc_smem(uint8_t* smem) {
+  TcSmem sm;
+  sm.ring = smem;
+  sm.T = reinterpret_cast<float*>(smem + kTcStages * kTcStageBytes);
+  sm.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm.T) +
+                                        ((kLinRows * (kTcMP + 1) * sizeof(float) + 15) & ~size_t(15)));
+  sm.xnorm = sm.full + kTcStages;
+  sm.empty = sm.xnorm + kTcStages;
+  sm.acc_full = sm.empty + kTcStages;
+  sm.acc_empty = sm.acc_full + 2;
+  sm.drain = sm.acc_empty + 2;
+  sm.gbar = sm.drain + 1;
+  sm.gs = reinterpret_cast<bf16*>(sm.gbar + 1);
+  sm.s_rstd = reinterpret_cast<float*>(sm.gs + kLinXCols);
+  sm.s_hrstd = sm.s_rstd + kMaxK;
+  sm.taddr = reinterpret_cast<uint32_t*>(sm.s_hrstd + 64);
+  return sm;
+}
+
+// ---------------------------------------------------------------- producer
+// One thread.  The weight boxes of the first S blocks go out before the wait
+// on the previous kernel (weights never depend on it), their input boxes
+// after it; then both for each block as its stage frees up.  Returns the
+// number of blocks issued through `issued` and false on a timeout.
+__device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CUtensorMap* xmap, int cta,
+                           int G, const TcSmem& sm, long long& issued) {
+  const int KB = p.Kd / kLinBK;
+  long long kb_begin, kb_end;
+  lin_range(p, cta, G, kb_begin, kb_end);
+  const long long n = kb_end - kb_begin;
+  const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+  issued = 0;
+  if (n <= 0) return true;
+  int tile = (int)(kb_begin / KB), kk = (int)(kb_begin % KB);
+  auto weight = [&](int s) {
+    const TileRows tr = tile_rows(p, tile);
+    uint8_t* dst = sm.ring + s * kTcStageBytes;
+    tma_load_2d(dst, wmap, kk * kLinBK, tr.a0, &sm.full[s], pol_w);
+    tma_load_2d(dst + kLinChunkBytes, wmap, kk * kLinBK, tr.b0, &sm.full[s], pol_w);
+  };
+  auto input = [&](int s, int kcol) {
+    tma_load_2d(sm.ring + s * kTcStageBytes + kLinStageBytes, xmap, kcol * kLinBK, 0, &sm.full[s], pol_x);
+  };
+  auto advance = [&]() {
+    if (++kk == KB) {
+      kk = 0;
+      ++tile;
+    }
+  };
+  const int pre = (int)(n < kTcStages ? n : kTcStages);
+  const int kk_first = kk;
+  for (int s = 0; s < pre; ++s) {
+    mbar_arrive_expect_tx(&sm.full[s], kTcStageBytes);
+    weight(s);
+    advance();
+  }
+  pdl_wait();  // the input rows come from the previous kernel
+  for (int s = 0, kc = kk_first; s < pre; ++s) {
+    input(s, kc);
+    if (++kc == KB) kc = 0;
+  }
+  issued = pre;
+  for (long long i = pre; i < n; ++i) {
+    const int s = (int)(i % kTcStages);
+    if (!mbar_wait(&sm.empty[s], (uint32_t)((i / kTcStages) & 1) ^ 1u)) return false;
+    mbar_arrive_expect_tx(&sm.full[s], kTcStageBytes);
+    weight(s);
+    input(s, kk);
+    advance();
+    issued = i + 1;
+  }
+  return true;
+}
+
+// Wait (bounded) until the copies of the last use of every stage landed.
+__device__ void tc_produce_drain(const TcSmem& sm, long long issued) {
+  for (long long u = issued - 1; u >= 0 && u >= issued - kTcStages; --u)
+    mbar_wait(&sm.full[u % kTcStages], (uint32_t)((u / kTcStages) & 1));
+}
+
+// ---------------------------------------------------------------- MMA issuer
+// One thread: per block, wait for its bytes (and, with a norm prologue, for
+// the normalised input rows), then four k16 multiplies; the stage is released
+// when they complete, the accumulator when the piece's last ones complete.
+template <bool NORM>
+__device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, uint32_t tmem) {
+  const int KB = p.Kd / kLinBK;
+  long long kb_begin, kb_end;
+  lin_range(p, cta, G, kb_begin, kb_end);
+  constexpr uint32_t idesc = tc_idesc(kLinRows, kTcMP);
+  long long left = kb_end - kb_begin;
+  int kk0 = (int)(kb_begin % KB);
+  long long it = 0;
+  int piece = 0;
+  bool ok = true;
+  while (left > 0 && ok) {
+    const int nblk = (int)(left < KB - kk0 ? left : KB - kk0);
+    const int b = piece & 1;
+    if (piece >= 2 && !mbar_wait(&sm.acc_empty[b], (uint32_t)((piece / 2) & 1) ^ 1u)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem + (uint32_t)(b * kTcMP);
+    for (int j = 0; j < nblk; ++j, ++it) {
+      const int s = (int)(it % kTcStages);
+      const uint32_t par = (uint32_t)((it / kTcStages) & 1);
+      if (!mbar_wait(&sm.full[s], par) || (NORM && !mbar_wait(&sm.xnorm[s], par))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(sm.ring + s * kTcStageBytes), b_base = a_base + kLinStageBytes;
+#pragma unroll
+      for (int k16 = 0; k16 < kLinBK / 16; ++k16)
+        tc_mma(d_tmem, tc_sdesc(a_base + 32 * k16), tc_sdesc(b_base + 32 * k16), idesc, j > 0 || k16 > 0);
+      tc_commit(&sm.empty[s]);
+    }
+    if (!ok) break;
+    tc_commit(&sm.acc_full[b]);
+    ++piece;
+    left -= nblk;
+    kk0 = 0;
+  }
+  // every multiply this thread issued has completed before tensor memory is freed
+  tc_commit(sm.drain);
+  if (!mbar_wait(sm.drain, 0)) ok = false;
+  return ok;
+}
+
+// ---------------------------------------------------------------- consumers
+// A CTA's partial slot holds 128 x 32 words, token rows paired and tile rows
+// innermost: the pair (c, c + 1), c even, of tile row lr is at words
+// 2 (64 c + lr) and + 1, so a warp (32 consecutive tile rows) stores and
+// polls 512 contiguous bytes per instruction.
+__device__ __forceinline__ unsigned long long* tc_pair(unsigned long long* slot, int lr, int c) {
+  return slot + 2 * (64 * c + lr);
+}
+
+// Split-tile reducer: v holds this CTA's piece (segment 0) of the 16 values
+// at tile row lr, token rows mb .. mb + 15; add the partials that CTAs
+// cta + 1 ... cta + nseg - 1 left in their slots, in segment order, two
+// segments per polling round, and clear the words.
+__device__ __forceinline__ bool tc_gather(unsigned long long* ws, int cta, int nseg, int lr, int mb, int M,
+                                          float (&v)[16]) {
+  constexpr int B = 2, NP = 8 * B;
+  bool ok = true;
+  for (int j0 = 1; j0 < nseg; j0 += B) {
+    auto addr = [&](int i) {
+      return tc_pair(ws + (size_t)(cta + j0 + i / 8) * kLinRows * kTcMP, lr, mb + 2 * (i % 8));
+    };
+    unsigned long long x[NP], y[NP];
+    uint32_t live = 0;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      x[i] = y[i] = 0ull;
+      if (j0 + i / 8 < nseg && mb + 2 * (i % 8) < M) {  // pairs of padding rows are not exchanged
+        live |= 1u << i;
+        ld_relaxed_v2_u64(addr(i), x[i], y[i]);
+      }
+    }
+    if (!poll_pairs<NP>(addr, x, y, live)) ok = false;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      if ((live >> i) & 1u) {
+        const int c = 2 * (i % 8);
+        v[c] = __fadd_rn(v[c], __uint_as_float((uint32_t)x[i]));
+        v[c + 1] = __fadd_rn(v[c + 1], __uint_as_float((uint32_t)y[i]));
+        st_relaxed_v2_u64(addr(i), 0ull, 0ull);
+      }
+    }
+  }
+  return ok;
+}
+
+// Row rstd of the input from the per-128-column partial sums of squares, in
+// the mma.sync form's order (lane-strided sums, then an xor tree); warp w
+// takes rows w + 8 k, all four rows' loads in flight together.
+__device__ __forceinline__ void tc_row_rstd(const LinParams& p, const TcSmem& sm, int warp, int lane) {
+  constexpr int R = kTcMP / kLinConsumerWarps;
+  float ss[R];
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int m = warp + kLinConsumerWarps * k;
+    ss[k] = 0.0f;
+    if (m < p.M)
+      for (int t = lane; t < p.ss_tiles; t += 32) ss[k] = __fadd_rn(ss[k], __ldcg(p.x_ss + m * p.ss_tiles + t));
+  }
+#pragma unroll
+  for (int k = 0; k < R; ++k) {
+    const int m = warp + kLinConsumerWarps * k;
+    for (int o = 16; o > 0; o >>= 1) ss[k] = __fadd_rn(ss[k], __shfl_xor_sync(0xffffffffu, ss[k], o));
+    if (lane == 0 && m < p.M) sm.s_rstd[m] = 1.0f / sqrtf(ss[k] / (float)p.Kd + p.eps);
+  }
+}
+
+template <int EPI, bool NORM>
+__device__ bool tc_consume(const LinParams& p, int cta, int G, const TcSmem& sm, uint32_t tmem) {
+  constexpr int MP = kTcMP, TS = MP + 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nthr = kLinConsumerWarps * 32;
+  const int KB = p.Kd / kLinBK;
+  const long long Tk = (long long)p.n_tiles * KB;
+  long long kb_begin, kb_end;
+  lin_range(p, cta, G, kb_begin, kb_end);
+  if (kb_begin >= kb_end) return true;
+  // The gain of the input window (columns c0 + t mod Kd, t < ncols) does not
+  // depend on earlier kernels: staged before the wait when it fits.
+  int c0 = 0, ncols = 0;
+  lin_window(p, kb_begin, kb_end, c0, ncols);
+  const bool gain_staged = NORM && ncols <= kLinXCols;
+  if (gain_staged && tid == 0) {
+    const int first = min(ncols, p.Kd - c0);
+    mbar_arrive_expect_tx(sm.gbar, (uint32_t)(ncols * sizeof(bf16)));
+    bulk_load(sm.gs, p.gain + c0, (uint32_t)(first * sizeof(bf16)), sm.gbar);
+    if (first < ncols) bulk_load(sm.gs + first, p.gain, (uint32_t)((ncols - first) * sizeof(bf16)), sm.gbar);
+  }
+  pdl_wait();  // sums of squares, the step state and the residual come from earlier kernels
+  int pos = 0, cap = 0;
+  if (EPI == EPI_QKV) {
+    pos = __ldcg(&p.st->step_pos);
+    cap = __ldcg(&p.st->cap_len);
+  }
+  bool ok = true;
+  if (NORM) {
+    tc_row_rstd(p, sm, warp, lane);
+    if (gain_staged && !mbar_wait(sm.gbar, 0)) ok = false;
+    named_sync(1, nthr);
+  }
+  // accumulator read-back: warp w owns tensor-memory lanes (tile rows)
+  // 32 (w mod 4) + lane and token rows mb .. mb + 15
+  const int lr = 32 * (warp & 3) + lane, mb = 16 * (warp >> 2);
+  float* T = sm.T;
+  EpiPre<MP> pre;
+  long long it = 0;
+  int piece = 0;
+  int tile = (int)(kb_begin / KB), kk0 = (int)(kb_begin % KB);
+  long long left = kb_end - kb_begin;
+  while (left > 0) {
+    const int nblk = (int)(left < KB - kk0 ? left : KB - kk0);
+    if (NORM) {
+      // block `it` is normalised by consumer warp it mod 8, so eight blocks
+      // are in hand at once; lane l takes the 16-byte chunk l mod 8 of rows
+      // 4 i + l / 8 (four rows of 128 contiguous bytes per access: no bank
+      // conflicts).  128B swizzle: chunk pc of row m holds columns
+      // 8 (pc ^ (m mod 8)) .. + 7 of the block.
+      for (int j = 0; j < nblk; ++j, ++it) {
+        if ((int)(it % kLinConsumerWarps) != warp) continue;
+        const int s = (int)(it % kTcStages);
+        if (ok && !mbar_wait(&sm.full[s], (uint32_t)((it / kTcStages) & 1))) ok = false;
+        if (ok) {
+          uint8_t* xb = sm.ring + s * kTcStageBytes + kLinStageBytes;
+          const int pc = lane & 7;
+          int wc = (kk0 + j) * kLinBK - c0;  // window column of the block
+          if (wc < 0) wc += p.Kd;
+          const uint4* g = gain_staged ? reinterpret_cast<const uint4*>(sm.gs + wc)
+                                       : reinterpret_cast<const uint4*>(p.gain + (kk0 + j) * kLinBK);
+#pragma unroll
+          for (int i = 0; i < kTcMP / 4; ++i) {
+            const int m = 4 * i + (lane >> 3);
+            if (m < p.M) {
+              uint4* ptr = reinterpret_cast<uint4*>(xb + m * 128 + pc * 16);
+              const int gc = pc ^ (m & 7);
+              *ptr = norm8(*ptr, sm.s_rstd[m], gain_staged ? g[gc] : __ldg(g + gc));
+            }
+          }
+        }
+        fence_proxy_async_smem();  // the multiplies read these rows through the async proxy
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.xnorm[s]);
+      }
+    }
+    // ------------ this CTA's piece of the tile is complete (k-blocks kk0 .. kk0 + nblk - 1)
+    const int kk = kk0 + nblk - 1, kk_first = kk0, tile_done = tile;
+    left -= nblk;
+    ++tile;
+    kk0 = 0;
+    float v[16];
+    const int b = piece & 1;
+    if (ok && !mbar_wait(&sm.acc_full[b], (uint32_t)((piece / 2) & 1))) ok = false;
+    tc_fence_after();
+    if (ok) {
+      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(b * MP + mb);
+      tc_ld8(ta, v);
+      tc_ld8(ta + 8, v + 8);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] = 0.0f;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+    ++piece;
+    if (kk_first != 0) {
+      // A later segment of a split tile (the first piece of this CTA's
+      // range): leave the partial in this CTA's slot, tagged, and move on.
+      unsigned long long* slot = p.ws + (size_t)cta * kLinRows * MP;
+#pragma unroll
+      for (int c = 0; c < 16; c += 2)
+        if (mb + c < p.M) st_relaxed_v2_u64(tc_pair(slot, lr, mb + c), tagged(v[c]), tagged(v[c + 1]));
+      continue;
+    }
+    epi_preload<MP, EPI>(p, tile_done, pos, cap, pre);
+    if (kk != KB - 1) {
+      // The first segment of a split tile (the last piece of this CTA's
+      // range): add the later segments' partials in k order.
+      const int nseg = owner_cta((long long)tile_done * KB + KB - 1, Tk, G) - cta + 1;
+      if (!tc_gather(p.ws, cta, nseg, lr, mb, p.M, v)) ok = false;
+    }
+    named_sync(1, nthr);  // the previous tile's epilogue is done with T
+#pragma unroll
+    for (int c = 0; c < 16; ++c) T[lr * TS + mb + c] = v[c];
+    named_sync(1, nthr);
+    if (EPI == EPI_QKV)
+      epilogue_qkv<MP>(p, tile_done, T, TS, sm.s_hrstd, pos, pre);
+    else if (EPI == EPI_RESID)
+      epilogue_resid<MP>(p, tile_done, T, TS, pre);
+    else if (EPI == EPI_GLU)
+      epilogue_glu(p, tile_done, T, TS);
+    else
+      epilogue_logits<MP>(p, tile_done, T, TS);
+  }
+  return ok;
+}
+
+// Persistent stream-K linear, same partition as k_linear (one CTA per SM,
+// equal contiguous k-block ranges, split tiles finished by their first CTA).
+template <int EPI, bool NORM>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_linear_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap pfmap,
+                const __grid_constant__ CUtensorMap xmap, const LinParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const TcSmem sm = tc_smem(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.xnorm[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], kLinConsumerWarps);
+    }
+    mbar_init(sm.drain, 1);
+    mbar_init(sm.gbar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {  // one warp allocates (and later frees) the two accumulators
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sm.taddr)),
+                 "n"(kTcCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sm.taddr;
+  pdl_trigger();  // the next kernel may start its own weight stream
+  bool ok = true;
+  if (warp == kTcProducerWarp) {
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&xmap);
+      long long issued = 0;
+      ok = tc_produce(p, &wmap, &xmap, blockIdx.x, gridDim.x, sm, issued);
+      if (ok) lin_prefetch_next(p, &pfmap, blockIdx.x);
+      tc_produce_drain(sm, issued);
+    }
+  } else if (warp == kTcMmaWarp) {
+    if (lane == 0) ok = tc_issue<NORM>(p, blockIdx.x, gridDim.x, sm, tmem);
+  } else {
+    ok = tc_consume<EPI, NORM>(p, blockIdx.x, gridDim.x, sm, tmem);
+  }
+  if (!ok && lane == 0) atomicOr(&p.st->status, ST_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcCols) : "memory");
+  }
+}
+
+template <int EPI, bool NORM>
+cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, const LinParams& p, cudaStream_t s,
+                        bool pdl, const CUtensorMap& pfmap) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(d.grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = linear_tc_smem_bytes();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM>, d.map, pfmap, xmap, p);
+}
+
+template <int EPI, bool NORM>
+cudaError_t prepare_tc_t() {
+  return cudaFuncSetAttribute(k_linear_tc<EPI, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)linear_tc_smem_bytes());
+}
+
+}  // namespace
+
+size_t linear_tc_smem_bytes() {
+  size_t b = 1024;  // alignment slack
+  b += (size_t)kTcStages * kTcStageBytes;
+  b += ((size_t)kLinRows * (kTcMP + 1) * sizeof(float) + 15) & ~size_t(15);
+  b += (3 * kTcStages + 6) * sizeof(uint64_t) + kLinXCols * sizeof(bf16) + (kMaxK + 64) * sizeof(float) + 16;
+  return b;
+}
+
+cudaError_t prepare_linear_tc_kernels() {
+  cudaError_t e;
+  if ((e = prepare_tc_t<EPI_QKV, true>()) != cudaSuccess) return e;
+  if ((e = prepare_tc_t<EPI_RESID, false>()) != cudaSuccess) return e;
+  if ((e = prepare_tc_t<EPI_GLU, true>()) != cudaSuccess) return e;
+  return prepare_tc_t<EPI_LOGITS, true>();
+}
+
+cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, const LinParams& p_in, int epi,
+                             bool norm, cudaStream_t s, bool pdl, const LinearDesc* next) {
+  if (p_in.M < 1 || p_in.M > kTcMP) return cudaErrorInvalidValue;
+  LinParams p = p_in;
+  if (next) {
+    p.pf_blocks = kLinPrefetchBlocks;
+    p.pf_n_tiles = next->n_tiles;
+    p.pf_Kd = next->Kd;
+    p.pf_grid = next->grid;
+    p.pf_map = next->map_kind;
+    p.pf_ffn = next->N / 2;  // gate|up: the up rows start at ffn
+  } else {
+    p.pf_blocks = 0;
+  }
+  const CUtensorMap& pf = next ? next->map : d.map;
+  switch (epi) {
+    case EPI_QKV:
+      return norm ? launch_tc_t<EPI_QKV, true>(d, xmap, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_RESID:
+      return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false>(d, xmap, p, s, pdl, pf);
+    case EPI_GLU:
+      return norm ? launch_tc_t<EPI_GLU, true>(d, xmap, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_LOGITS:
+      return norm ? launch_tc_t<EPI_LOGITS, true>(d, xmap, p, s, pdl, pf) : cudaErrorInvalidValue;
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace sv

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "sv_internal.h"
+#include "linear_tc.h"
 
 using namespace sv;
 
@@ -28,6 +29,7 @@ struct sv_ctx {
   cudaEvent_t ev = nullptr;
   bool use_graphs = true;
   bool use_pdl = true;  // chain a step's kernels with programmatic dependent launch
+  bool use_tc = true;   // 17-32 row linears on tcgen05 (bit-identical to the mma.sync form)
   int prefetch_mode = 0;  // 0 none, 1 every linear prefetches the next one into L2, 2 only QKV -> O
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
@@ -35,6 +37,7 @@ struct sv_ctx {
   std::vector<LinearDesc> lin_qkv, lin_o, lin_gu, lin_down;
   LinearDesc lin_head;
   CUtensorMap kmap, vmap;
+  CUtensorMap xmap_x, xmap_o, xmap_a;  // input rows of the linears, [kMaxK rows] x 64-column boxes
   // device memory owned by the context
   std::vector<void*> allocs;
   bf16 *kpool = nullptr, *vpool = nullptr;
@@ -145,6 +148,16 @@ int dalloc(sv_ctx* ctx, T** p, size_t count) {
 }
 
 int mp_of(int M) { return M <= 8 ? 8 : (M <= 16 ? 16 : 32); }
+
+// One linear of a step: blocks of more than 16 rows go to the tcgen05 form.
+cudaError_t run_linear(sv_ctx* ctx, const LinearDesc& d, const LinParams& p, int epi, bool norm,
+                       cudaStream_t s, bool pdl, const LinearDesc* next) {
+  if (ctx->use_tc && p.M > 16) {
+    const CUtensorMap* xm = p.X == ctx->x ? &ctx->xmap_x : (p.X == ctx->o ? &ctx->xmap_o : &ctx->xmap_a);
+    return launch_linear_tc(d, *xm, p, epi, norm, s, pdl, next);
+  }
+  return launch_linear(d, p, epi, norm, s, pdl, next);
+}
 
 // ------------------------------------------------------------------ the step
 enum LinWhich { LIN_QKV = 0, LIN_O = 1, LIN_GU = 2, LIN_DOWN = 3, LIN_HEAD = 4 };
@@ -279,18 +292,18 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   };
   for (int l = 0; l < c.n_layers; ++l) {
     LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
-    CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_QKV, l)));
+    CK(run_linear(ctx, *ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_QKV, l)));
     AttnParams ap = attn_params(ctx, l, M);
     CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, ctx->use_pdl));
     CK(launch_attn_combine(ap, d, s, ctx->use_pdl));
     for (int w : {LIN_O, LIN_GU, LIN_DOWN}) {
       p = lin_params(ctx, w, l, M, mode, logits, &epi, &norm, &ld);
-      CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(w, l)));
+      CK(run_linear(ctx, *ld, p, epi, norm, s, ctx->use_pdl, next_of(w, l)));
     }
   }
   if (head) {  // final RMSNorm + LM head + per-tile argmax
     LinParams p = lin_params(ctx, LIN_HEAD, 0, M, mode, logits, &epi, &norm, &ld);
-    CK(launch_linear(*ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_HEAD, 0)));
+    CK(run_linear(ctx, *ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_HEAD, 0)));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
                    ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s,
@@ -456,7 +469,10 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   // prefetches compete with the slowest CTAs of the current launch).
   const char* pf = getenv("SV_L2_PREFETCH");
   ctx->prefetch_mode = pf ? atoi(pf) : 0;
-  if (prepare_linear_kernels() != cudaSuccess || prepare_attention_kernels() != cudaSuccess)
+  const char* nt = getenv("SV_NO_TC");
+  ctx->use_tc = !(nt && nt[0] == '1');
+  if (prepare_linear_kernels() != cudaSuccess || prepare_linear_tc_kernels() != cudaSuccess ||
+      prepare_attention_kernels() != cudaSuccess)
     return bail(SV_E_CUDA);
 
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
@@ -523,7 +539,9 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
   if (!make_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
-      !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage))
+      !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
+      !make_map(&ctx->xmap_x, ctx->x, kMaxK, H, kMaxK) || !make_map(&ctx->xmap_o, ctx->o, kMaxK, Hq * d, kMaxK) ||
+      !make_map(&ctx->xmap_a, ctx->a, kMaxK, c.ffn, kMaxK))
     return bail(SV_E_CUDA);
   // a prefill of max_seq tokens stages every block [cap_len, tokens] side by side
   ctx->pin_in_len = (size_t)c.max_seq + (c.max_seq + kMaxK - 1) / kMaxK + kMaxK + 8;
@@ -810,7 +828,7 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
         next = which == SV_LIN_O ? &ctx->lin_o[ln]
                                  : (which == SV_LIN_GATE_UP ? &ctx->lin_gu[ln] : &ctx->lin_down[ln]);
       }
-      CK(launch_linear(*ld, p, epi, norm, ctx->stream, !(r == 0 && l == 0), next));
+      CK(run_linear(ctx, *ld, p, epi, norm, ctx->stream, !(r == 0 && l == 0), next));
       if (r == 0) {
         const double n_out = which == SV_LIN_GATE_UP ? (double)c.ffn : (double)ld->N;
         bytes += 2.0 * ld->N * ld->Kd + 2.0 * K * ld->Kd + 2.0 * K * n_out;
