@@ -212,7 +212,11 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
     for (int j = 0; j < nblk; ++j, ++it) {
       const int s = (int)(it % kTcStages);
       const uint32_t par = (uint32_t)((it / kTcStages) & 1);
-      if (!mbar_wait(&sm.full[s], par) || (NORM && !mbar_wait(&sm.xnorm[s], par))) {
+      if (!mbar_wait(&sm.full[s], par)) {
+        ok = false;
+        break;
+      }
+      if (NORM && !mbar_wait(&sm.xnorm[s], par)) {
         ok = false;
         break;
       }
@@ -236,44 +240,85 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
 }
 
 // ---------------------------------------------------------------- consumers
-// A CTA's partial slot holds 128 x 32 words, token rows paired and tile rows
-// innermost: the pair (c, c + 1), c even, of tile row lr is at words
-// 2 (64 c + lr) and + 1, so a warp (32 consecutive tile rows) stores and
-// polls 512 contiguous bytes per instruction.
-__device__ __forceinline__ unsigned long long* tc_pair(unsigned long long* slot, int lr, int c) {
-  return slot + 2 * (64 * c + lr);
+// Split-tile exchange.  A CTA's partial slot holds 128 x 32 fp32 words,
+// token rows in quads and tile rows innermost: the quad (c .. c + 3), c a
+// multiple of 4, of tile row lr is at words 4 (32 c + lr) .. + 3, so a warp
+// (32 consecutive tile rows) stores and polls 512 contiguous bytes per
+// instruction.  A word not yet written holds kTcEmpty, a NaN with the sign
+// bit set: arithmetic only produces the canonical NaN 0x7fffffff, so no
+// partial sum is ever equal to it.  Quads of padding rows (c >= M) are not
+// exchanged.  The reducer puts kTcEmpty back into every word it consumed.
+constexpr uint32_t kTcEmpty = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t* tc_quad(uint32_t* slot, int lr, int c) { return slot + 4 * (32 * c + lr); }
+
+__device__ __forceinline__ void st_relaxed_v4_u32(uint32_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_v4_u32(const uint32_t* p, uint4& v) {
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
 }
 
 // Split-tile reducer: v holds this CTA's piece (segment 0) of the 16 values
 // at tile row lr, token rows mb .. mb + 15; add the partials that CTAs
-// cta + 1 ... cta + nseg - 1 left in their slots, in segment order, two
-// segments per polling round, and clear the words.
-__device__ __forceinline__ bool tc_gather(unsigned long long* ws, int cta, int nseg, int lr, int mb, int M,
+// cta + 1 ... cta + nseg - 1 left in their slots, in segment order, four
+// segments per polling round.  Returns false if a partial never arrived.
+__device__ __forceinline__ bool tc_gather(uint32_t* slots, int cta, int nseg, int lr, int mb, int M,
                                           float (&v)[16]) {
-  constexpr int B = 2, NP = 8 * B;
+  constexpr int B = 4, NQ = 4 * B;  // quad i: segment j0 + i / 4, token rows mb + 4 (i mod 4) ..
   bool ok = true;
   for (int j0 = 1; j0 < nseg; j0 += B) {
     auto addr = [&](int i) {
-      return tc_pair(ws + (size_t)(cta + j0 + i / 8) * kLinRows * kTcMP, lr, mb + 2 * (i % 8));
+      return tc_quad(slots + (size_t)(cta + j0 + i / 4) * kLinRows * kTcMP, lr, mb + 4 * (i % 4));
     };
-    unsigned long long x[NP], y[NP];
+    uint4 x[NQ];
     uint32_t live = 0;
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
-      x[i] = y[i] = 0ull;
-      if (j0 + i / 8 < nseg && mb + 2 * (i % 8) < M) {  // pairs of padding rows are not exchanged
+    for (int i = 0; i < NQ; ++i) {
+      x[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (j0 + i / 4 < nseg && mb + 4 * (i % 4) < M) {
         live |= 1u << i;
-        ld_relaxed_v2_u64(addr(i), x[i], y[i]);
+        ld_relaxed_v4_u32(addr(i), x[i]);
       }
     }
-    if (!poll_pairs<NP>(addr, x, y, live)) ok = false;
+    auto missing = [&]() {
+      uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
+      for (int i = 0; i < NQ; ++i)
+        if (((live >> i) & 1u) &&
+            (x[i].x == kTcEmpty || x[i].y == kTcEmpty || x[i].z == kTcEmpty || x[i].w == kTcEmpty))
+          m |= 1u << i;
+      return m;
+    };
+    uint32_t m = missing();
+    if (m != 0) {
+      const unsigned long long t0 = globaltimer_ns();
+      for (;;) {
+#pragma unroll
+        for (int i = 0; i < NQ; ++i)
+          if ((m >> i) & 1u) ld_relaxed_v4_u32(addr(i), x[i]);
+        m = missing();
+        if (m == 0) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NQ; ++i) {
       if ((live >> i) & 1u) {
-        const int c = 2 * (i % 8);
-        v[c] = __fadd_rn(v[c], __uint_as_float((uint32_t)x[i]));
-        v[c + 1] = __fadd_rn(v[c + 1], __uint_as_float((uint32_t)y[i]));
-        st_relaxed_v2_u64(addr(i), 0ull, 0ull);
+        const int c = 4 * (i % 4);
+        v[c] = __fadd_rn(v[c], __uint_as_float(x[i].x));
+        v[c + 1] = __fadd_rn(v[c + 1], __uint_as_float(x[i].y));
+        v[c + 2] = __fadd_rn(v[c + 2], __uint_as_float(x[i].z));
+        v[c + 3] = __fadd_rn(v[c + 3], __uint_as_float(x[i].w));
+        st_relaxed_v4_u32(addr(i), kTcEmpty, kTcEmpty, kTcEmpty, kTcEmpty);
       }
     }
   }
@@ -302,7 +347,7 @@ __device__ __forceinline__ void tc_row_rstd(const LinParams& p, const TcSmem& sm
 }
 
 template <int EPI, bool NORM>
-__device__ bool tc_consume(const LinParams& p, int cta, int G, const TcSmem& sm, uint32_t tmem) {
+__device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, const TcSmem& sm, uint32_t tmem) {
   constexpr int MP = kTcMP, TS = MP + 1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nthr = kLinConsumerWarps * 32;
@@ -401,10 +446,12 @@ __device__ bool tc_consume(const LinParams& p, int cta, int G, const TcSmem& sm,
     if (kk_first != 0) {
       // A later segment of a split tile (the first piece of this CTA's
       // range): leave the partial in this CTA's slot, tagged, and move on.
-      unsigned long long* slot = p.ws + (size_t)cta * kLinRows * MP;
+      uint32_t* slot = slots + (size_t)cta * kLinRows * MP;
 #pragma unroll
-      for (int c = 0; c < 16; c += 2)
-        if (mb + c < p.M) st_relaxed_v2_u64(tc_pair(slot, lr, mb + c), tagged(v[c]), tagged(v[c + 1]));
+      for (int c = 0; c < 16; c += 4)
+        if (mb + c < p.M)
+          st_relaxed_v4_u32(tc_quad(slot, lr, mb + c), __float_as_uint(v[c]), __float_as_uint(v[c + 1]),
+                            __float_as_uint(v[c + 2]), __float_as_uint(v[c + 3]));
       continue;
     }
     epi_preload<MP, EPI>(p, tile_done, pos, cap, pre);
@@ -412,7 +459,7 @@ __device__ bool tc_consume(const LinParams& p, int cta, int G, const TcSmem& sm,
       // The first segment of a split tile (the last piece of this CTA's
       // range): add the later segments' partials in k order.
       const int nseg = owner_cta((long long)tile_done * KB + KB - 1, Tk, G) - cta + 1;
-      if (!tc_gather(p.ws, cta, nseg, lr, mb, p.M, v)) ok = false;
+      if (!tc_gather(slots, cta, nseg, lr, mb, p.M, v)) ok = false;
     }
     named_sync(1, nthr);  // the previous tile's epilogue is done with T
 #pragma unroll
@@ -435,7 +482,7 @@ __device__ bool tc_consume(const LinParams& p, int cta, int G, const TcSmem& sm,
 template <int EPI, bool NORM>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_linear_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap pfmap,
-                const __grid_constant__ CUtensorMap xmap, const LinParams p) {
+                const __grid_constant__ CUtensorMap xmap, const LinParams p, uint32_t* slots) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -479,7 +526,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kTcMmaWarp) {
     if (lane == 0) ok = tc_issue<NORM>(p, blockIdx.x, gridDim.x, sm, tmem);
   } else {
-    ok = tc_consume<EPI, NORM>(p, blockIdx.x, gridDim.x, sm, tmem);
+    ok = tc_consume<EPI, NORM>(p, slots, blockIdx.x, gridDim.x, sm, tmem);
   }
   if (!ok && lane == 0) atomicOr(&p.st->status, ST_TIMEOUT);
   tc_fence_before();
@@ -491,8 +538,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 }
 
 template <int EPI, bool NORM>
-cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, const LinParams& p, cudaStream_t s,
-                        bool pdl, const CUtensorMap& pfmap) {
+cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p,
+                        cudaStream_t s, bool pdl, const CUtensorMap& pfmap) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.grid);
   cfg.blockDim = dim3(kTcThreads);
@@ -503,7 +550,7 @@ cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, const LinP
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM>, d.map, pfmap, xmap, p);
+  return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM>, d.map, pfmap, xmap, p, slots);
 }
 
 template <int EPI, bool NORM>
@@ -530,8 +577,8 @@ cudaError_t prepare_linear_tc_kernels() {
   return prepare_tc_t<EPI_LOGITS, true>();
 }
 
-cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, const LinParams& p_in, int epi,
-                             bool norm, cudaStream_t s, bool pdl, const LinearDesc* next) {
+cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p_in,
+                             int epi, bool norm, cudaStream_t s, bool pdl, const LinearDesc* next) {
   if (p_in.M < 1 || p_in.M > kTcMP) return cudaErrorInvalidValue;
   LinParams p = p_in;
   if (next) {
@@ -547,13 +594,13 @@ cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, const
   const CUtensorMap& pf = next ? next->map : d.map;
   switch (epi) {
     case EPI_QKV:
-      return norm ? launch_tc_t<EPI_QKV, true>(d, xmap, p, s, pdl, pf) : cudaErrorInvalidValue;
+      return norm ? launch_tc_t<EPI_QKV, true>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
     case EPI_RESID:
-      return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false>(d, xmap, p, s, pdl, pf);
+      return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false>(d, xmap, slots, p, s, pdl, pf);
     case EPI_GLU:
-      return norm ? launch_tc_t<EPI_GLU, true>(d, xmap, p, s, pdl, pf) : cudaErrorInvalidValue;
+      return norm ? launch_tc_t<EPI_GLU, true>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
     case EPI_LOGITS:
-      return norm ? launch_tc_t<EPI_LOGITS, true>(d, xmap, p, s, pdl, pf) : cudaErrorInvalidValue;
+      return norm ? launch_tc_t<EPI_LOGITS, true>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }

@@ -11,8 +11,10 @@ size_t linear_tc_smem_bytes();
 cudaError_t prepare_linear_tc_kernels();
 // Same contract as launch_linear for 17 <= p.M <= 32, same grid and split,
 // bit-identical results.  xmap: tensor map of p.X ([32 rows, p.Kd] bf16,
-// row-major, box 32 rows x 64 columns, 128B swizzle).
-cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, const LinParams& p, int epi,
-                             bool norm, cudaStream_t s, bool pdl, const LinearDesc* next = nullptr);
+// row-major, box 32 rows x 64 columns, 128B swizzle).  slots: the split-tile
+// exchange of this form (p.ws is not used), d.grid x 128 x 32 32-bit words,
+// every byte 0xff before the first launch; each launch leaves them so.
+cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p,
+                             int epi, bool norm, cudaStream_t s, bool pdl, const LinearDesc* next = nullptr);
 
 }  // namespace sv

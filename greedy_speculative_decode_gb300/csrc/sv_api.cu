@@ -51,6 +51,7 @@ struct sv_ctx {
   float* part_o = nullptr;
   int max_splits = 0;
   unsigned long long* ws = nullptr;  // split-tile partial slots, one per CTA (tags start at 0)
+  uint32_t* ws_tc = nullptr;         // the same for the tcgen05 form (every byte 0xff when idle)
   float* am_val = nullptr;
   int* am_idx = nullptr;
   // pinned host staging
@@ -154,7 +155,7 @@ cudaError_t run_linear(sv_ctx* ctx, const LinearDesc& d, const LinParams& p, int
                        cudaStream_t s, bool pdl, const LinearDesc* next) {
   if (ctx->use_tc && p.M > 16) {
     const CUtensorMap* xm = p.X == ctx->x ? &ctx->xmap_x : (p.X == ctx->o ? &ctx->xmap_o : &ctx->xmap_a);
-    return launch_linear_tc(d, *xm, p, epi, norm, s, pdl, next);
+    return launch_linear_tc(d, *xm, ctx->ws_tc, p, epi, norm, s, pdl, next);
   }
   return launch_linear(d, p, epi, norm, s, pdl, next);
 }
@@ -534,10 +535,11 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->rope, (size_t)c.max_seq * (d / 2))) ||
       (rc = dalloc(ctx, &ctx->part_ml, (size_t)kMaxK * Hq * ctx->max_splits)) ||
       (rc = dalloc(ctx, &ctx->part_o, (size_t)kMaxK * Hq * ctx->max_splits * d)) ||
-      (rc = dalloc(ctx, &ctx->ws, ws_words)) ||
+      (rc = dalloc(ctx, &ctx->ws, ws_words)) || (rc = dalloc(ctx, &ctx->ws_tc, ws_words)) ||
       (rc = dalloc(ctx, &ctx->am_val, (size_t)kMaxK * ctx->lin_head.n_tiles)) ||
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
+  if (cudaMemset(ctx->ws_tc, 0xff, ws_words * sizeof(uint32_t)) != cudaSuccess) return bail(SV_E_CUDA);
   if (!make_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
       !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
       !make_map(&ctx->xmap_x, ctx->x, kMaxK, H, kMaxK) || !make_map(&ctx->xmap_o, ctx->o, kMaxK, Hq * d, kMaxK) ||
