@@ -1,12 +1,13 @@
-// k_linear_tc.cu -- the batch-invariant linear for blocks of 17 to 32 rows on
+// k_linear_tc.cu -- the batch-invariant linear for blocks of 9 to 32 rows on
 // the fifth-generation tensor cores (tcgen05): Y[m, n] = sum_k X[m, k] W[n, k].
 //
 // Same weight stream, split and epilogues as the mma.sync form, with the
 // multiply moved off the consumer warps.  Each ring stage holds a 128-row x
 // 64-column weight block (two TMA boxes) and the 32 x 64 block of the input
 // rows at the same columns (one TMA box; rows past M are never stored).  One
-// thread issues, per block, four tcgen05.mma of 128 x 32 x 16 (weight rows
-// as the 128-row operand, token rows as the 32-column one) into an fp32
+// thread issues, per block, four tcgen05.mma of 128 x N x 16 (weight rows as
+// the 128-row operand, the token rows padded to N = 16 or 32 as the N-column
+// one) into an fp32
 // accumulator in tensor memory; a tile piece (a CTA's run of k-blocks inside
 // one 128-row tile) starts from zero, two accumulators alternate so the next
 // piece runs while the consumers read the last one back.
@@ -29,12 +30,12 @@ namespace sv {
 namespace {
 
 constexpr int kTcStages = 8;
-constexpr int kTcMP = 32;                                  // padded token rows
+constexpr int kTcMP = 32;                                  // most padded token rows (the 32-row form)
 constexpr int kTcXBytes = kTcMP * 128;                     // 32 rows x 64 columns, 128B-swizzled
 constexpr int kTcStageBytes = kLinStageBytes + kTcXBytes;  // 20 KB, a multiple of 1024
 constexpr int kTcThreads = (kLinConsumerWarps + 2) * 32;
 constexpr int kTcProducerWarp = kLinConsumerWarps, kTcMmaWarp = kLinConsumerWarps + 1;
-constexpr int kTcCols = 2 * kTcMP;                         // tensor-memory columns: two accumulators
+constexpr int kTcCols = 2 * kTcMP;                         // tensor-memory columns: two accumulators of up to 32
 static_assert(kTcStageBytes % 1024 == 0, "swizzle atoms stay aligned");
 
 // ---------------------------------------------------------------- tcgen05
@@ -189,12 +190,12 @@ __device__ void tc_produce_drain(const TcSmem& sm, long long issued) {
 // One thread: per block, wait for its bytes (and, with a norm prologue, for
 // the normalised input rows), then four k16 multiplies; the stage is released
 // when they complete, the accumulator when the piece's last ones complete.
-template <bool NORM>
+template <bool NORM, int MP>
 __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, uint32_t tmem) {
   const int KB = p.Kd / kLinBK;
   long long kb_begin, kb_end;
   lin_range(p, cta, G, kb_begin, kb_end);
-  constexpr uint32_t idesc = tc_idesc(kLinRows, kTcMP);
+  constexpr uint32_t idesc = tc_idesc(kLinRows, MP);
   long long left = kb_end - kb_begin;
   int kk0 = (int)(kb_begin % KB);
   long long it = 0;
@@ -208,7 +209,7 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem + (uint32_t)(b * kTcMP);
+    const uint32_t d_tmem = tmem + (uint32_t)(b * kTcMP);  // buffers 32 columns apart
     for (int j = 0; j < nblk; ++j, ++it) {
       const int s = (int)(it % kTcStages);
       const uint32_t par = (uint32_t)((it / kTcStages) & 1);
@@ -264,24 +265,26 @@ __device__ __forceinline__ void ld_relaxed_v4_u32(const uint32_t* p, uint4& v) {
                : "memory");
 }
 
-// Split-tile reducer: v holds this CTA's piece (segment 0) of the 16 values
-// at tile row lr, token rows mb .. mb + 15; add the partials that CTAs
-// cta + 1 ... cta + nseg - 1 left in their slots, in segment order, four
-// segments per polling round.  Returns false if a partial never arrived.
+// Split-tile reducer: v holds this CTA's piece (segment 0) of the CW values
+// at tile row lr, token rows mb .. mb + CW - 1; add the partials that CTAs
+// cta + 1 ... cta + nseg - 1 left in their slots, in segment order, sixteen
+// quads (four segments of 32 rows, eight of 16) per polling round.  Returns
+// false if a partial never arrived.
+template <int CW>
 __device__ __forceinline__ bool tc_gather(uint32_t* slots, int cta, int nseg, int lr, int mb, int M,
-                                          float (&v)[16]) {
-  constexpr int B = 4, NQ = 4 * B;  // quad i: segment j0 + i / 4, token rows mb + 4 (i mod 4) ..
+                                          float (&v)[CW]) {
+  constexpr int QS = CW / 4, NQ = 16, B = NQ / QS;  // quad i: segment j0 + i / QS, rows mb + 4 (i mod QS) ..
   bool ok = true;
   for (int j0 = 1; j0 < nseg; j0 += B) {
     auto addr = [&](int i) {
-      return tc_quad(slots + (size_t)(cta + j0 + i / 4) * kLinRows * kTcMP, lr, mb + 4 * (i % 4));
+      return tc_quad(slots + (size_t)(cta + j0 + i / QS) * kLinRows * kTcMP, lr, mb + 4 * (i % QS));
     };
     uint4 x[NQ];
     uint32_t live = 0;
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
       x[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (j0 + i / 4 < nseg && mb + 4 * (i % 4) < M) {
+      if (j0 + i / QS < nseg && mb + 4 * (i % QS) < M) {
         live |= 1u << i;
         ld_relaxed_v4_u32(addr(i), x[i]);
       }
@@ -313,7 +316,7 @@ __device__ __forceinline__ bool tc_gather(uint32_t* slots, int cta, int nseg, in
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
       if ((live >> i) & 1u) {
-        const int c = 4 * (i % 4);
+        const int c = 4 * (i % QS);
         v[c] = __fadd_rn(v[c], __uint_as_float(x[i].x));
         v[c + 1] = __fadd_rn(v[c + 1], __uint_as_float(x[i].y));
         v[c + 2] = __fadd_rn(v[c + 2], __uint_as_float(x[i].z));
@@ -328,8 +331,9 @@ __device__ __forceinline__ bool tc_gather(uint32_t* slots, int cta, int nseg, in
 // Row rstd of the input from the per-128-column partial sums of squares, in
 // the mma.sync form's order (lane-strided sums, then an xor tree); warp w
 // takes rows w + 8 k, all four rows' loads in flight together.
+template <int MP>
 __device__ __forceinline__ void tc_row_rstd(const LinParams& p, const TcSmem& sm, int warp, int lane) {
-  constexpr int R = kTcMP / kLinConsumerWarps;
+  constexpr int R = MP / kLinConsumerWarps;
   float ss[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
@@ -346,9 +350,9 @@ __device__ __forceinline__ void tc_row_rstd(const LinParams& p, const TcSmem& sm
   }
 }
 
-template <int EPI, bool NORM>
+template <int EPI, bool NORM, int MP>
 __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, const TcSmem& sm, uint32_t tmem) {
-  constexpr int MP = kTcMP, TS = MP + 1;
+  constexpr int TS = MP + 1, CW = MP / 2;  // CW: token rows per consumer warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nthr = kLinConsumerWarps * 32;
   const int KB = p.Kd / kLinBK;
@@ -375,13 +379,13 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
   }
   bool ok = true;
   if (NORM) {
-    tc_row_rstd(p, sm, warp, lane);
+    tc_row_rstd<MP>(p, sm, warp, lane);
     if (gain_staged && !mbar_wait(sm.gbar, 0)) ok = false;
     named_sync(1, nthr);
   }
   // accumulator read-back: warp w owns tensor-memory lanes (tile rows)
-  // 32 (w mod 4) + lane and token rows mb .. mb + 15
-  const int lr = 32 * (warp & 3) + lane, mb = 16 * (warp >> 2);
+  // 32 (w mod 4) + lane and token rows mb .. mb + CW - 1
+  const int lr = 32 * (warp & 3) + lane, mb = CW * (warp >> 2);
   float* T = sm.T;
   EpiPre<MP> pre;
   long long it = 0;
@@ -408,7 +412,7 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
           const uint4* g = gain_staged ? reinterpret_cast<const uint4*>(sm.gs + wc)
                                        : reinterpret_cast<const uint4*>(p.gain + (kk0 + j) * kLinBK);
 #pragma unroll
-          for (int i = 0; i < kTcMP / 4; ++i) {
+          for (int i = 0; i < MP / 4; ++i) {
             const int m = 4 * i + (lane >> 3);
             if (m < p.M) {
               uint4* ptr = reinterpret_cast<uint4*>(xb + m * 128 + pc * 16);
@@ -427,17 +431,17 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
     left -= nblk;
     ++tile;
     kk0 = 0;
-    float v[16];
+    float v[CW];
     const int b = piece & 1;
     if (ok && !mbar_wait(&sm.acc_full[b], (uint32_t)((piece / 2) & 1))) ok = false;
     tc_fence_after();
     if (ok) {
-      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(b * MP + mb);
-      tc_ld8(ta, v);
-      tc_ld8(ta + 8, v + 8);
+      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(b * kTcMP + mb);
+#pragma unroll
+      for (int c = 0; c < CW; c += 8) tc_ld8(ta + c, v + c);
     } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) v[c] = 0.0f;
+      for (int c = 0; c < CW; ++c) v[c] = 0.0f;
     }
     tc_fence_before();
     __syncwarp();
@@ -446,9 +450,9 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
     if (kk_first != 0) {
       // A later segment of a split tile (the first piece of this CTA's
       // range): leave the partial in this CTA's slot, tagged, and move on.
-      uint32_t* slot = slots + (size_t)cta * kLinRows * MP;
+      uint32_t* slot = slots + (size_t)cta * kLinRows * kTcMP;
 #pragma unroll
-      for (int c = 0; c < 16; c += 4)
+      for (int c = 0; c < CW; c += 4)
         if (mb + c < p.M)
           st_relaxed_v4_u32(tc_quad(slot, lr, mb + c), __float_as_uint(v[c]), __float_as_uint(v[c + 1]),
                             __float_as_uint(v[c + 2]), __float_as_uint(v[c + 3]));
@@ -459,11 +463,11 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
       // The first segment of a split tile (the last piece of this CTA's
       // range): add the later segments' partials in k order.
       const int nseg = owner_cta((long long)tile_done * KB + KB - 1, Tk, G) - cta + 1;
-      if (!tc_gather(slots, cta, nseg, lr, mb, p.M, v)) ok = false;
+      if (!tc_gather<CW>(slots, cta, nseg, lr, mb, p.M, v)) ok = false;
     }
     named_sync(1, nthr);  // the previous tile's epilogue is done with T
 #pragma unroll
-    for (int c = 0; c < 16; ++c) T[lr * TS + mb + c] = v[c];
+    for (int c = 0; c < CW; ++c) T[lr * TS + mb + c] = v[c];
     named_sync(1, nthr);
     if (EPI == EPI_QKV)
       epilogue_qkv<MP>(p, tile_done, T, TS, sm.s_hrstd, pos, pre);
@@ -479,7 +483,7 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
 
 // Persistent stream-K linear, same partition as k_linear (one CTA per SM,
 // equal contiguous k-block ranges, split tiles finished by their first CTA).
-template <int EPI, bool NORM>
+template <int EPI, bool NORM, int MP>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_linear_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap pfmap,
                 const __grid_constant__ CUtensorMap xmap, const LinParams p, uint32_t* slots) {
@@ -524,9 +528,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_produce_drain(sm, issued);
     }
   } else if (warp == kTcMmaWarp) {
-    if (lane == 0) ok = tc_issue<NORM>(p, blockIdx.x, gridDim.x, sm, tmem);
+    if (lane == 0) ok = tc_issue<NORM, MP>(p, blockIdx.x, gridDim.x, sm, tmem);
   } else {
-    ok = tc_consume<EPI, NORM>(p, slots, blockIdx.x, gridDim.x, sm, tmem);
+    ok = tc_consume<EPI, NORM, MP>(p, slots, blockIdx.x, gridDim.x, sm, tmem);
   }
   if (!ok && lane == 0) atomicOr(&p.st->status, ST_TIMEOUT);
   tc_fence_before();
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-template <int EPI, bool NORM>
+template <int EPI, bool NORM, int MP>
 cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p,
                         cudaStream_t s, bool pdl, const CUtensorMap& pfmap) {
   cudaLaunchConfig_t cfg = {};
@@ -550,13 +554,32 @@ cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM>, d.map, pfmap, xmap, p, slots);
+  return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM, MP>, d.map, pfmap, xmap, p, slots);
 }
 
 template <int EPI, bool NORM>
 cudaError_t prepare_tc_t() {
-  return cudaFuncSetAttribute(k_linear_tc<EPI, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k_linear_tc<EPI, NORM, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)linear_tc_smem_bytes());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_linear_tc<EPI, NORM, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)linear_tc_smem_bytes());
+}
+
+template <int MP>
+cudaError_t launch_tc_mp(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p,
+                         int epi, bool norm, cudaStream_t s, bool pdl, const CUtensorMap& pf) {
+  switch (epi) {
+    case EPI_QKV:
+      return norm ? launch_tc_t<EPI_QKV, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_RESID:
+      return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false, MP>(d, xmap, slots, p, s, pdl, pf);
+    case EPI_GLU:
+      return norm ? launch_tc_t<EPI_GLU, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_LOGITS:
+      return norm ? launch_tc_t<EPI_LOGITS, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -592,17 +615,8 @@ cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, uint3
     p.pf_blocks = 0;
   }
   const CUtensorMap& pf = next ? next->map : d.map;
-  switch (epi) {
-    case EPI_QKV:
-      return norm ? launch_tc_t<EPI_QKV, true>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
-    case EPI_RESID:
-      return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false>(d, xmap, slots, p, s, pdl, pf);
-    case EPI_GLU:
-      return norm ? launch_tc_t<EPI_GLU, true>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
-    case EPI_LOGITS:
-      return norm ? launch_tc_t<EPI_LOGITS, true>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
-  }
-  return cudaErrorInvalidValue;
+  if (p.M <= 16) return launch_tc_mp<16>(d, xmap, slots, p, epi, norm, s, pdl, pf);
+  return launch_tc_mp<32>(d, xmap, slots, p, epi, norm, s, pdl, pf);
 }
 
 }  // namespace sv

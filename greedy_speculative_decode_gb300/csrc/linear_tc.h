@@ -1,5 +1,5 @@
 // linear_tc.h -- host side of the tcgen05 form of the batch-invariant linear,
-// used for blocks of 17 to 32 rows.
+// used for blocks of 9 to 32 rows.
 #pragma once
 #include "sv_internal.h"
 
@@ -9,7 +9,8 @@ namespace sv {
 size_t linear_tc_smem_bytes();
 // Raise the shared-memory limit of every variant (once per process is enough).
 cudaError_t prepare_linear_tc_kernels();
-// Same contract as launch_linear for 17 <= p.M <= 32, same grid and split,
+// Same contract as launch_linear for 1 <= p.M <= 32 (rows padded to 16 or 32),
+// same grid and split,
 // bit-identical results.  xmap: tensor map of p.X ([32 rows, p.Kd] bf16,
 // row-major, box 32 rows x 64 columns, 128B swizzle).  slots: the split-tile
 // exchange of this form (p.ws is not used), d.grid x 128 x 32 32-bit words,

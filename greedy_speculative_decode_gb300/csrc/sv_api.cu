@@ -29,7 +29,7 @@ struct sv_ctx {
   cudaEvent_t ev = nullptr;
   bool use_graphs = true;
   bool use_pdl = true;  // chain a step's kernels with programmatic dependent launch
-  bool use_tc = true;   // 17-32 row linears on tcgen05 (bit-identical to the mma.sync form)
+  bool use_tc = true;   // 9-32 row linears on tcgen05 (bit-identical to the mma.sync form)
   int prefetch_mode = 0;  // 0 none, 1 every linear prefetches the next one into L2, 2 only QKV -> O
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
@@ -150,10 +150,10 @@ int dalloc(sv_ctx* ctx, T** p, size_t count) {
 
 int mp_of(int M) { return M <= 8 ? 8 : (M <= 16 ? 16 : 32); }
 
-// One linear of a step: blocks of more than 16 rows go to the tcgen05 form.
+// One linear of a step: blocks of more than 8 rows go to the tcgen05 form.
 cudaError_t run_linear(sv_ctx* ctx, const LinearDesc& d, const LinParams& p, int epi, bool norm,
                        cudaStream_t s, bool pdl, const LinearDesc* next) {
-  if (ctx->use_tc && p.M > 16) {
+  if (ctx->use_tc && p.M > 8) {
     const CUtensorMap* xm = p.X == ctx->x ? &ctx->xmap_x : (p.X == ctx->o ? &ctx->xmap_o : &ctx->xmap_a);
     return launch_linear_tc(d, *xm, ctx->ws_tc, p, epi, norm, s, pdl, next);
   }

@@ -1,4 +1,4 @@
-"""The tcgen05 form of the linear (blocks of 17 to 32 rows) against the
+"""The tcgen05 form of the linear (blocks of 9 to 32 rows) against the
 mma.sync form: the same prefill and verify steps on two contexts, one with the
 tcgen05 form switched off (SV_NO_TC=1), give byte-identical logits, K/V,
 acceptance and corrections.  Run on the full-width 0.6B-, 8B- and Gemma-like
@@ -38,7 +38,7 @@ def _same_cache(cfg, a, b):
         assert torch.equal(va.view(torch.int16), vb.view(torch.int16)), layer
 
 
-@pytest.mark.parametrize("K", [17, 24, 32])
+@pytest.mark.parametrize("K", [9, 12, 16, 17, 24, 32])
 def test_verify_identical_with_and_without_tcgen05(model, monkeypatch, K):
     cfg, dw = model
     prompt = inputs.prefix_tokens(40 + K, 300 + K, cfg.vocab)  # prefill: 32-row blocks and a ragged one
@@ -61,11 +61,12 @@ def test_verify_identical_with_and_without_tcgen05(model, monkeypatch, K):
         pending = r_tc[1]
 
 
-def test_rows_of_a_32_row_block_equal_decode(model, monkeypatch):
-    """Each row of a 32-row all-accept verify on the tcgen05 form equals the
-    single-token decode of its prefix (mma.sync, one token row), bit for bit."""
+@pytest.mark.parametrize("K", [16, 32])
+def test_rows_of_a_wide_block_equal_decode(model, monkeypatch, K):
+    """Each row of a 16- or 32-row all-accept verify on the tcgen05 form
+    equals the single-token decode of its prefix (mma.sync, one token row),
+    bit for bit."""
     cfg, dw = model
-    K = 32
     prompt = inputs.prefix_tokens(91, 70, cfg.vocab)
     dec = gh.context(cfg, dw, max_k=32, max_seq=70 + K + 8)
     lg1 = gh.logits_buf(1, cfg.vocab)
