@@ -401,6 +401,10 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
       // conflicts).  128B swizzle: chunk pc of row m holds columns
       // 8 (pc ^ (m mod 8)) .. + 7 of the block.
       for (int j = 0; j < nblk; ++j, ++it) {
+        // Every use of stage s then has the same owner, warp s: a warp never
+        // waits on a stage's barrier two phases ahead, where the parity
+        // test would alias and pass early.  That needs one warp per stage.
+        static_assert(kTcStages == kLinConsumerWarps, "one owner warp per ring stage");
         if ((int)(it % kLinConsumerWarps) != warp) continue;
         const int s = (int)(it % kTcStages);
         if (ok && !mbar_wait(&sm.full[s], (uint32_t)((it / kTcStages) & 1))) ok = false;
