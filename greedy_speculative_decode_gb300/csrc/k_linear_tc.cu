@@ -7,10 +7,9 @@
 // rows at the same columns (one TMA box; rows past M are never stored).  One
 // thread issues, per block, four tcgen05.mma of 128 x N x 16 (weight rows as
 // the 128-row operand, the token rows padded to N = 16 or 32 as the N-column
-// one) into an fp32
-// accumulator in tensor memory; a tile piece (a CTA's run of k-blocks inside
-// one 128-row tile) starts from zero, two accumulators alternate so the next
-// piece runs while the consumers read the last one back.
+// one) into an fp32 accumulator in tensor memory; a tile piece (a CTA's run
+// of k-blocks inside one 128-row tile) starts from zero, and two accumulators
+// alternate so the next piece runs while the consumers read the last one back.
 //
 // Bit-identity with the mma.sync form (and so with single-token decode):
 // every output element is the fp32 sum of the same products taken 16 k at a
@@ -453,7 +452,8 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
     ++piece;
     if (kk_first != 0) {
       // A later segment of a split tile (the first piece of this CTA's
-      // range): leave the partial in this CTA's slot, tagged, and move on.
+      // range): leave the partial in this CTA's slot (its words were empty)
+      // and move on.
       uint32_t* slot = slots + (size_t)cta * kLinRows * kTcMP;
 #pragma unroll
       for (int c = 0; c < CW; c += 4)
