@@ -89,7 +89,18 @@ typedef struct {
  * stream (cudaStream_t) or NULL for the legacy stream; the library orders its
  * own internal stream after it at the start of each call and the caller's
  * stream after the library's work at the end.  Allocates the KV pool, block
- * table, activations and workspaces (all owned by the context). */
+ * table, activations and workspaces (all owned by the context).
+ *
+ * Environment switches, read here (results are bit-identical whichever are
+ * set; they change only how the work is launched):
+ *   SV_NO_TC=1        steps of 9..32 rows use the mma.sync linear instead of
+ *                     the tcgen05 one;
+ *   SV_NO_GRAPHS=1    launch every step's kernels directly instead of through
+ *                     a CUDA graph per (rows, mode, logits buffer);
+ *   SV_NO_PDL=1       no programmatic dependent launch between a step's kernels;
+ *   SV_L2_PREFETCH=n  1: each linear prefetches the next one's first k-blocks
+ *                     into L2; 2: only the QKV linear does, for the attention
+ *                     projection (off by default: it measured slower). */
 int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_ctx** out);
 void sv_destroy(sv_ctx* ctx);
 
