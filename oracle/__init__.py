@@ -49,6 +49,9 @@ def _open(path: str):
     L.orc_truncate.argtypes = [_P, i32]
     L.orc_kv.argtypes = [_P, i32, i32, _P, _P]
     L.orc_bruteforce.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), _P, i32, _P]
+    L.orc_layer.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), i32, i32, i32, _P, _P,
+                            _P, _P, _P, _P]
+    L.orc_head.argtypes = [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), _P, _P]
     L.orc_bf16.argtypes = [f32]
     L.orc_bf16.restype = u16
     L.orc_f32.argtypes = [u16]
@@ -62,6 +65,7 @@ def _open(path: str):
     L.orc_silu.restype = f32
     L.orc_gelu_tanh.argtypes = [f32]
     L.orc_gelu_tanh.restype = f32
+    L.orc_glu.argtypes = [_P, _P, i32, i32, _P]
     return L
 
 
@@ -142,6 +146,13 @@ def silu(x: float) -> float:
 
 def gelu_tanh(x: float) -> float:
     return float(lib().orc_gelu_tanh(x))
+
+
+def glu(gate_bits, up_bits, act: int) -> np.ndarray:
+    g, u = _u16(gate_bits), _u16(up_bits)
+    a = np.empty_like(g)
+    lib().orc_glu(_ptr(g), _ptr(u), g.size, int(act), _ptr(a))
+    return a
 
 
 def threads() -> int:
@@ -257,3 +268,48 @@ def bruteforce(hw, tokens) -> np.ndarray:
     if rc != 0:
         raise ValueError("bruteforce rejected its arguments")
     return lg
+
+
+class LayerOracle:
+    """One layer, or the final head, of the oracle applied to given inputs:
+    the per-token pass cut at a layer boundary (teacher forcing)."""
+
+    def __init__(self, hw):
+        self.hw = hw
+        self._b = _Bound(hw)
+
+    def layer(self, layer: int, pos: int, x_in, k_cache=None, v_cache=None):
+        """Rows x_in (bf16 bits [K, hidden]) at positions pos .. pos+K-1 through
+        layer ``layer``, over that layer's cached K/V of positions 0 .. pos-1
+        (bf16 bits [pos, n_kv_heads * head_dim]). Returns (x_out, k, v): the
+        rows after the layer and their own K and V."""
+        c = self.hw.cfg
+        x = _u16(x_in).reshape(-1, c.hidden)
+        K = x.shape[0]
+        row = c.n_kv_heads * c.head_dim
+        kc = None if k_cache is None else _u16(k_cache).reshape(-1, row)
+        vc = None if v_cache is None else _u16(v_cache).reshape(-1, row)
+        if pos > 0 and (kc is None or vc is None or kc.shape[0] < pos or vc.shape[0] < pos):
+            raise ValueError("the cache must hold every position before pos")
+        xo = np.empty_like(x)
+        ko = np.empty((K, row), dtype=np.uint16)
+        vo = np.empty_like(ko)
+        rc = lib().orc_layer(ctypes.byref(self._b.cfg), ctypes.byref(self._b.w), int(layer), int(pos),
+                             K, 0 if kc is None else _ptr(kc), 0 if vc is None else _ptr(vc),
+                             _ptr(x), _ptr(xo), _ptr(ko), _ptr(vo))
+        if rc != 0:
+            raise ValueError("orc_layer rejected its arguments")
+        return xo, ko, vo
+
+    def head(self, x):
+        """Final RMSNorm + LM head of residual-stream rows x (bf16 bits [K, hidden]):
+        logits [K, vocab] (bf16 values)."""
+        c = self.hw.cfg
+        xs = _u16(x).reshape(-1, c.hidden)
+        out = np.empty((xs.shape[0], c.vocab), dtype=np.float32)
+        for r in range(xs.shape[0]):
+            xr = np.ascontiguousarray(xs[r])
+            if lib().orc_head(ctypes.byref(self._b.cfg), ctypes.byref(self._b.w), _ptr(xr),
+                              _ptr(out[r])) != 0:
+                raise ValueError("orc_head rejected its arguments")
+        return out

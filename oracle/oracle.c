@@ -124,6 +124,14 @@ float orc_gelu_tanh(float x) {
   return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
 }
 
+void orc_glu(const uint16_t* gate, const uint16_t* up, int n, int act, uint16_t* a) {
+  for (int i = 0; i < n; ++i) {
+    float g = orc_f32(gate[i]), u = orc_f32(up[i]);
+    float y = act == 0 ? orc_silu(g) : orc_gelu_tanh(g);
+    a[i] = orc_bf16(rb(y) * u);
+  }
+}
+
 /* ------------------------------------------------------------ model state */
 struct orc_model {
   orc_config c;
@@ -249,11 +257,7 @@ static void layer_rest(const orc_config* c, const orc_weights* w, int l, int pos
   for (int i = 0; i < H; ++i) t->x[i] = orc_bf16(orc_f32(t->x[i]) + orc_f32(t->att[i]));
   orc_rmsnorm(t->x, w->ffn_norm[l], H, c->rms_eps, t->y);
   orc_linear(w->w_gate_up[l], t->y, 2 * F, H, t->gu);
-  for (int i = 0; i < F; ++i) {
-    float g = orc_f32(t->gu[i]), u = orc_f32(t->gu[F + i]);
-    float act = c->act == 0 ? orc_silu(g) : orc_gelu_tanh(g);
-    t->a[i] = orc_bf16(rb(act) * u);
-  }
+  orc_glu(t->gu, t->gu + F, F, c->act, t->a);
   orc_linear(w->w_down[l], t->a, H, F, t->dn);
   for (int i = 0; i < H; ++i) t->x[i] = orc_bf16(orc_f32(t->x[i]) + orc_f32(t->dn[i]));
 }
@@ -345,6 +349,48 @@ int orc_kv(const orc_model* m, int layer, int pos, uint16_t* k_out, uint16_t* v_
   size_t off = ((size_t)layer * m->max_len + pos) * row;
   if (k_out) memcpy(k_out, m->kc + off, 2 * row);
   if (v_out) memcpy(v_out, m->vc + off, 2 * row);
+  return 0;
+}
+
+/* The per-token pass of orc_forward cut at one layer: the rows run one after
+ * another in position order, each writing its own K/V before it attends, so
+ * row r sees the given cache and rows 0 .. r. */
+int orc_layer(const orc_config* c, const orc_weights* w, int layer, int pos, int K,
+              const uint16_t* k_cache, const uint16_t* v_cache, const uint16_t* x_in,
+              uint16_t* x_out, uint16_t* k_out, uint16_t* v_out) {
+  if (!cfg_ok(c) || !w || layer < 0 || layer >= c->n_layers || pos < 0 || K <= 0 || !x_in || !x_out)
+    return -1;
+  if (pos > 0 && (!k_cache || !v_cache)) return -1;
+  size_t row = kv_row(c), H = (size_t)c->hidden;
+  uint16_t* kb = (uint16_t*)malloc(2 * (size_t)(pos + K) * row);
+  uint16_t* vb = (uint16_t*)malloc(2 * (size_t)(pos + K) * row);
+  if (pos > 0) {
+    memcpy(kb, k_cache, 2 * (size_t)pos * row);
+    memcpy(vb, v_cache, 2 * (size_t)pos * row);
+  }
+  orc_tmp t;
+  tmp_init(&t, c);
+  for (int r = 0; r < K; ++r) {
+    memcpy(t.x, x_in + (size_t)r * H, 2 * H);
+    layer_qkv(c, w, layer, pos + r, &t, kb + (size_t)(pos + r) * row, vb + (size_t)(pos + r) * row);
+    layer_rest(c, w, layer, pos + r, &t, kb, vb);
+    memcpy(x_out + (size_t)r * H, t.x, 2 * H);
+  }
+  if (k_out) memcpy(k_out, kb + (size_t)pos * row, 2 * (size_t)K * row);
+  if (v_out) memcpy(v_out, vb + (size_t)pos * row, 2 * (size_t)K * row);
+  tmp_free(&t);
+  free(kb);
+  free(vb);
+  return 0;
+}
+
+int orc_head(const orc_config* c, const orc_weights* w, const uint16_t* x, float* logits) {
+  if (!cfg_ok(c) || !w || !x || !logits) return -1;
+  orc_tmp t;
+  tmp_init(&t, c);
+  memcpy(t.x, x, 2 * (size_t)c->hidden);
+  final_logits(c, w, &t, logits);
+  tmp_free(&t);
   return 0;
 }
 

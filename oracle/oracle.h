@@ -69,6 +69,21 @@ int orc_kv(const orc_model* m, int layer, int pos, uint16_t* k_out, uint16_t* v_
 int orc_bruteforce(const orc_config* cfg, const orc_weights* w, const int32_t* tokens, int n,
                    float* logits);
 
+/* -------- one layer / the head on given inputs (teacher forcing) -------- */
+/* Layer `layer` applied to K consecutive rows at positions pos .. pos+K-1,
+ * given that layer's cached K and V of positions 0 .. pos-1 (k_cache, v_cache:
+ * [pos][n_kv_heads * head_dim] bf16 bits, may be NULL when pos = 0).  Row r
+ * attends to the given cache plus the keys of rows 0 .. r, exactly as a decode
+ * at position pos+r would.  x_in, x_out: [K][hidden] (the residual stream
+ * before and after the layer); k_out, v_out: [K][n_kv_heads * head_dim] (the
+ * rows' own cached K and V) or NULL. */
+int orc_layer(const orc_config* cfg, const orc_weights* w, int layer, int pos, int K,
+              const uint16_t* k_cache, const uint16_t* v_cache, const uint16_t* x_in,
+              uint16_t* x_out, uint16_t* k_out, uint16_t* v_out);
+/* Final RMSNorm + LM head of one residual-stream row x [hidden]: logits [vocab]
+ * (fp32 holding bf16 values). */
+int orc_head(const orc_config* cfg, const orc_weights* w, const uint16_t* x, float* logits);
+
 /* -------- single operations, exposed so tests can pin them -------- */
 uint16_t orc_bf16(float x);
 float orc_f32(uint16_t b);
@@ -82,6 +97,9 @@ void orc_attend(const uint16_t* q, const uint16_t* K, const uint16_t* V, int ctx
                 int stride, uint16_t* out);
 float orc_silu(float x);
 float orc_gelu_tanh(float x);
+/* Gated unit of one row: a[i] = bf16(bf16(act(gate[i])) * up[i]), act 0 = silu,
+ * 1 = tanh-approximated GELU. */
+void orc_glu(const uint16_t* gate, const uint16_t* up, int n, int act, uint16_t* a);
 
 #ifdef __cplusplus
 }

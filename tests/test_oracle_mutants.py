@@ -26,8 +26,15 @@ MUTANTS = {
     "gqa_head_map": ("int kvh = h / group;", "int kvh = h % Hkv;"),
     "context_off_by_one": ("pos + 1,\n               d, stride", "pos,\n               d, stride"),
     "no_score_scale": ("s[j] = dot * scale;", "s[j] = dot;"),
-    "gate_up_swapped": ("float g = orc_f32(t->gu[i]), u = orc_f32(t->gu[F + i]);",
-                        "float u = orc_f32(t->gu[i]), g = orc_f32(t->gu[F + i]);"),
+    "gate_up_swapped": ("orc_glu(t->gu, t->gu + F, F, c->act, t->a);",
+                        "orc_glu(t->gu + F, t->gu, F, c->act, t->a);"),
+    # the two intermediate bf16 roundings of the stated rounding path
+    "rmsnorm_intermediate_round_dropped": (
+        "y[i] = orc_bf16(rb(orc_f32(x[i]) * rstd) * orc_f32(g[i]));",
+        "y[i] = orc_bf16(orc_f32(x[i]) * rstd * orc_f32(g[i]));"),
+    "glu_activation_round_dropped": ("a[i] = orc_bf16(rb(y) * u);", "a[i] = orc_bf16(y * u);"),
+    "layer_entry_cache_offset": ("layer_rest(c, w, layer, pos + r, &t, kb, vb);",
+                                 "layer_rest(c, w, layer, pos + r, &t, kb + row, vb + row);"),
     "norm_gain_dropped": ("y[i] = orc_bf16(rb(orc_f32(x[i]) * rstd) * orc_f32(g[i]));",
                           "y[i] = orc_bf16(rb(orc_f32(x[i]) * rstd));"),
     "accept_compares_wrong_row": ("while (n < K - 1 && tokens[n + 1] == am[n]) ++n;",
@@ -43,6 +50,9 @@ BATTERY = [
     lambda: pins.test_model_matches_float64_library_decoder(0.1, 0, 1),
     lambda: pins.test_model_matches_float64_library_decoder(0.1, 1, 0),
     lambda: pins.test_rmsnorm_constant_vector(),
+    lambda: pins.test_rmsnorm_rounding_points_match_library_casts(),
+    lambda: pins.test_glu_rounding_points_match_library_casts(0),
+    lambda: pins.test_glu_rounding_points_match_library_casts(1),
     lambda: pins.test_linear_matches_matmul(),
     lambda: pins.test_rope_basis_vectors(64, 1e4),
     lambda: pins.test_rope_depends_on_relative_position_only(),
@@ -53,6 +63,7 @@ BATTERY = [
       for r in pins._rows("p3_position60_table.txt")],
     lambda: pins.test_verify_rows_equal_decode_and_accept_longest_prefix(_tiny()),
     lambda: pins.test_truncate_then_continue_equals_fresh(_tiny()),
+    lambda: pins.test_layer_entry_chain_equals_verify(_tiny()),
 ]
 
 _TINY = None

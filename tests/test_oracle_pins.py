@@ -115,6 +115,55 @@ def test_rmsnorm_matches_torch():
     assert np.all(np.abs(y - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
 
 
+def _bf16_equal_fraction(got_bits, ref64):
+    """Fraction of bf16 outputs equal to a float64 reference cast to bf16 by
+    the library (torch's own round-to-nearest-even), and the largest gap in
+    bf16 steps."""
+    ref = torch.from_numpy(np.asarray(ref64, dtype=np.float64)).to(torch.bfloat16)
+    ref_bits = ref.view(torch.int16).numpy().view(np.uint16)
+    got = np.asarray(got_bits, dtype=np.uint16)
+    # bf16 values of one sign are ordered like their bit patterns
+    gap = np.abs(got.astype(np.int64) - ref_bits.astype(np.int64))
+    same_sign = (got >> 15) == (ref_bits >> 15)
+    return float(np.mean(got == ref_bits)), int(np.max(np.where(same_sign, gap, 0)))
+
+
+def test_rmsnorm_rounding_points_match_library_casts():
+    """The stated rounding path of the RMSNorm, bf16(bf16(x * rstd) * g), against
+    float64 library arithmetic (F.rms_norm) cast to bf16 by the library at the
+    same two points.  The oracle's fp32 intermediates differ from float64 by
+    an fp32 rounding, which moves a bf16 result only near a rounding boundary:
+    a few outputs in a thousand.  Dropping either rounding moves a large
+    share of them (the gains are not 1)."""
+    rng = np.random.default_rng(11)
+    n = 4096
+    x = _bits(rng.normal(0, 2.0, n))
+    g = _bits(rng.uniform(0.5, 1.5, n))
+    xf = torch.from_numpy(oracle.bits_to_f32(x).astype(np.float64))
+    gf = torch.from_numpy(oracle.bits_to_f32(g).astype(np.float64))
+    t = F.rms_norm(xf, (n,), eps=1e-6).to(torch.bfloat16).to(torch.float64)
+    ref = (t * gf).numpy()
+    frac, gap = _bf16_equal_fraction(oracle.rmsnorm(x, g, 1e-6), ref)
+    assert frac >= 0.99 and gap <= 1, (frac, gap)
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_glu_rounding_points_match_library_casts(act):
+    """The gated unit's stated rounding path, bf16(bf16(act(g)) * u), against
+    float64 F.silu / F.gelu(tanh) with the library's bf16 casts at the same
+    points (same reasoning as the RMSNorm case)."""
+    rng = np.random.default_rng(12 + act)
+    n = 4096
+    gb = _bits(rng.normal(0, 1.3, n))
+    ub = _bits(rng.normal(0, 1.3, n))
+    gf = torch.from_numpy(oracle.bits_to_f32(gb).astype(np.float64))
+    uf = torch.from_numpy(oracle.bits_to_f32(ub).astype(np.float64))
+    a = F.silu(gf) if act == 0 else F.gelu(gf, approximate="tanh")
+    ref = (a.to(torch.bfloat16).to(torch.float64) * uf).numpy()
+    frac, gap = _bf16_equal_fraction(oracle.glu(gb, ub, act), ref)
+    assert frac >= 0.99 and gap <= 1, (act, frac, gap)
+
+
 def test_linear_matches_matmul():
     rng = np.random.default_rng(2)
     W = _bits(rng.normal(0, 0.05, (37, 300)))
@@ -328,6 +377,36 @@ def test_k1_verify_equals_decode(tiny):
     lg, am, n, c = a.verify([t])
     ld, nd = b.decode(t)
     assert n == 0 and c == nd and np.array_equal(lg[0], ld)
+
+
+def test_layer_entry_chain_equals_verify(tiny):
+    """The per-layer entry (one layer on given rows over a given cache) and the
+    head entry, chained over every layer from the embedded rows with the
+    model's own cache, reproduce the whole-model verify bit for bit: logits
+    and the window's K/V."""
+    cfg, hw = tiny
+    prompt = inputs.prefix_tokens(4, 21, cfg.vocab)
+    m = oracle.OracleModel(hw, 64)
+    _, t = m.prefill(prompt)
+    chain = [t]
+    for _ in range(4):
+        chain.append(m.decode(chain[-1])[1])
+    m.truncate(len(prompt))
+    window = chain[:4]  # the greedy chain: every draft accepted, so its K/V stay committed
+    lo, _, n, _ = m.verify(window)
+    assert n == 3
+    lay = oracle.LayerOracle(hw)
+    pos, row = len(prompt), cfg.n_kv_heads * cfg.head_dim
+    x = np.stack([hw.get("embed")[tok] for tok in window])
+    for l in range(cfg.n_layers):
+        kc = np.stack([m.kv(l, p)[0] for p in range(pos)])
+        vc = np.stack([m.kv(l, p)[1] for p in range(pos)])
+        x, k, v = lay.layer(l, pos, x, kc, vc)
+        for r in range(4):
+            mk, mv = m.kv(l, pos + r)
+            assert np.array_equal(k[r], mk) and np.array_equal(v[r], mv), (l, r)
+        assert k.shape == (4, row)
+    assert np.array_equal(lay.head(x), lo)
 
 
 def test_truncate_then_continue_equals_fresh(tiny):
