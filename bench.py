@@ -332,8 +332,11 @@ def audit(steps, first, count, every, prefix, K, vocab):
             ctx.prefill(sq["chain"][len(ctx) - prefix:i])
         ctx.verify(toks, lv)
         ctx.truncate(base)
+        pending = None  # unknown after the truncation
         for r, t in enumerate(toks):
-            ctx.decode(t, ld)
+            # the decode of row r's prefix: a draft that is not the pending
+            # greedy token goes in as a one-token prefill (same kernels, M = 1)
+            pending = ctx.decode(t, ld) if pending is None or t == pending else ctx.prefill([t], ld)
             rows += 1
             if torch.equal(lv[r], ld[0]):
                 equal += 1

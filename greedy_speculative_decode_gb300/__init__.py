@@ -62,6 +62,7 @@ def _load():
     L.sv_seq_len.argtypes = [_P]
     L.sv_kv_read.argtypes = [_P, _i32, _i32, _i32, _P, _P]
     L.sv_shuffle_pages.argtypes = [_P, ctypes.c_uint64]
+    L.sv_trace_hidden.argtypes = [_P, _P, _i32]
     L.sv_step_kernel_count.argtypes = [_P, _i32, _i32]
     L.sv_spec_generate.argtypes = [_P, _P, _i32, _i32, _i32, _P, _P, _P, _P]
     L.sv_time_linear.argtypes = [_P, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_float),
@@ -71,7 +72,7 @@ def _load():
     L.sv_last_error.restype = ctypes.c_char_p
     for name in ("sv_create", "sv_prefill", "sv_decode", "sv_verify", "sv_verify_async",
                  "sv_reserve", "sv_sync", "sv_truncate", "sv_seq_len", "sv_kv_read",
-                 "sv_shuffle_pages", "sv_step_kernel_count", "sv_time_linear",
+                 "sv_shuffle_pages", "sv_trace_hidden", "sv_step_kernel_count", "sv_time_linear",
                  "sv_lm_head_noalloc"):
         getattr(L, name).restype = _i32
     return L
@@ -93,14 +94,40 @@ def _ptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def _check_tensor(t, name, dtype, shape):
+    """The C call takes raw pointers and cannot check what they point to: a
+    wrong dtype, shape, device or layout here would become out-of-bounds
+    device accesses there."""
+    if t is None:
+        return
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if str(t.dtype) != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
 def lm_head_noalloc(x, gain, w, logits, argmax=None, status=None, eps=1e-6, stream=None):
     """sv_lm_head_noalloc: logits and greedy tokens of M rows without any
     device allocation by the library (scratch is a fixed array inside it).
     x: bf16 [M, hidden]; gain: bf16 [hidden]; w: bf16 [vocab, hidden];
     logits: fp32 [M, vocab]; argmax: int32 [M] or None; status: int32 [1] or
-    None. All CUDA tensors owned by the caller. Asynchronous on `stream`."""
+    None. All CUDA tensors owned by the caller, contiguous. Asynchronous on
+    `stream`. Raises ValueError before any device work if a tensor does not
+    match these shapes and types."""
+    if getattr(x, "dim", lambda: 0)() != 2 or getattr(w, "dim", lambda: 0)() != 2:
+        raise ValueError("x and w must be 2-D tensors")
     M, hidden = int(x.shape[0]), int(x.shape[1])
     vocab = int(w.shape[0])
+    _check_tensor(x, "x", "torch.bfloat16", (M, hidden))
+    _check_tensor(gain, "gain", "torch.bfloat16", (hidden,))
+    _check_tensor(w, "w", "torch.bfloat16", (vocab, hidden))
+    _check_tensor(logits, "logits", "torch.float32", (M, vocab))
+    _check_tensor(argmax, "argmax", "torch.int32", (M,))
+    _check_tensor(status, "status", "torch.int32", (1,))
     s = _P(stream.cuda_stream) if stream is not None else _P(0)
     rc = _lib.sv_lm_head_noalloc(_P(_ptr(x)), _P(_ptr(gain)), _P(_ptr(w)), M, hidden, vocab,
                                  float(eps), _P(_ptr(logits)), _P(_ptr(argmax)), _P(_ptr(status)), s)
@@ -222,6 +249,15 @@ class Context:
 
     def shuffle_pages(self, seed: int):
         self._check(_lib.sv_shuffle_pages(self._h, ctypes.c_uint64(seed)))
+
+    def trace_hidden(self, buf, max_rows: int = 0):
+        """Test hook: while ``buf`` (bf16 CUDA [n_layers + 1, rows, hidden]
+        for steps of up to ``max_rows`` rows) is set, every step copies its
+        residual stream after each layer into it; None turns it off."""
+        if buf is not None:
+            _check_tensor(buf, "trace", "torch.bfloat16", (self.cfg.n_layers + 1, max_rows, self.cfg.hidden))
+        self._check(_lib.sv_trace_hidden(self._h, _P(_ptr(buf)), int(max_rows)))
+        self._trace = buf  # keep it alive while the library may write it
 
     def time_linear(self, which: int, K: int, reps: int = 3):
         """(mean device us per launch, algorithmic bytes per launch) of one

@@ -7,14 +7,20 @@ namespace sv {
 namespace {
 
 // x[m, :] = E[token_m, :]; x_ss[m, t] = sum of squares of x[m, 128t .. 128t+127].
-// Also opens the step: step_pos = seq_len.
+// Also opens the step: step_pos = seq_len, and for a verify step (check) notes
+// whether tokens[0] differs from the pending greedy token, in which case the
+// accept kernel commits nothing.
 __global__ void __launch_bounds__(128) k_embed(const bf16* __restrict__ E, int hidden, int vocab,
                                                bf16* __restrict__ x, float* __restrict__ x_ss,
-                                               int ss_tiles, SvState* st) {
+                                               int ss_tiles, SvState* st, int check) {
   pdl_trigger();
   __shared__ float part[4];
   const int t = blockIdx.x, m = blockIdx.y, i = threadIdx.x;
-  if (t == 0 && m == 0 && i == 0) st->step_pos = st->seq_len;
+  if (t == 0 && m == 0 && i == 0) {
+    st->step_pos = st->seq_len;
+    const int pending = st->pending;
+    st->step_reject = (check && pending >= 0 && st->tokens[0] != pending) ? 1 : 0;
+  }
   embed_tile(E, hidden, vocab, x, x_ss, ss_tiles, st, m, t, i, part, 3);
 }
 
@@ -91,10 +97,11 @@ __global__ void k_kv_gather(const bf16* kpool, const bf16* vpool, size_t layer_s
   }
 }
 
-__global__ void k_set_len(SvState* st, int len, int cap_len) {
+__global__ void k_set_len(SvState* st, int len, int cap_len, int pending) {
   st->seq_len = len;
   st->step_pos = len;
   if (cap_len >= 0) st->cap_len = cap_len;
+  if (pending != kKeepPending) st->pending = pending;
 }
 
 cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAttribute* attr,
@@ -113,8 +120,9 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAtt
 }  // namespace
 
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
-                         SvState* st, cudaStream_t s) {
-  k_embed<<<dim3(hidden / 128, M), 128, 0, s>>>(E, hidden, vocab, x, x_ss, hidden / 128, st);
+                         SvState* st, bool check, cudaStream_t s) {
+  k_embed<<<dim3(hidden / 128, M), 128, 0, s>>>(E, hidden, vocab, x, x_ss, hidden / 128, st,
+                                                check ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -151,8 +159,8 @@ cudaError_t launch_kv_gather(const bf16* kpool, const bf16* vpool, size_t layer_
   return cudaGetLastError();
 }
 
-cudaError_t launch_set_len(SvState* st, int len, int cap_len, cudaStream_t s) {
-  k_set_len<<<1, 1, 0, s>>>(st, len, cap_len);
+cudaError_t launch_set_len(SvState* st, int len, int cap_len, int pending, cudaStream_t s) {
+  k_set_len<<<1, 1, 0, s>>>(st, len, cap_len, pending);
   return cudaGetLastError();
 }
 

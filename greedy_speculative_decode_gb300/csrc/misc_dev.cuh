@@ -37,7 +37,10 @@ __device__ __forceinline__ void embed_tile(const bf16* __restrict__ E, int hidde
 // value, lowest id on ties), then acceptance: n = number of leading drafts
 // tokens[j+1] equal to argmax[j]; the row count committed is n + 1.  CTA 0
 // writes the results; the K/V of rejected rows are zeroed in layers
-// cta, cta + G_ctas, ...  Runs on 256 threads (named barrier 1).
+// cta, cta + G_ctas, ...  A verify step whose tokens[0] was not the pending
+// greedy token (step_reject) commits no row: every row of it is zeroed and
+// the length and pending token stay as they were.  Runs on 256 threads
+// (named barrier 1).
 __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                             int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                             const int* block_table, int n_layers, int n_kv_heads, int head_dim,
@@ -76,24 +79,34 @@ __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx,
     if (lane == 0) s_am[r] = bidx;
   }
   named_sync(1, 256);
+  const bool reject = mode == MODE_VERIFY && __ldcg(&st->step_reject) != 0;
   if (tid == 0) {
     int n = M - 1;
     if (mode == MODE_VERIFY) {
       n = 0;
       while (n < M - 1 && st->tokens[n + 1] == s_am[n]) ++n;
     }
-    *s_n = n;
+    *s_n = reject ? -1 : n;
   }
   named_sync(1, 256);
   const int n = *s_n;
-  const int new_len = pos + 1 + n;
+  const int new_len = pos + 1 + n;  // pos when the step is rejected
   if (cta == 0 && tid == 0) {
     for (int r = 0; r < M; ++r) st->argmax[r] = s_am[r];
     st->seq_len = new_len;
-    st->result[0] = n;
-    st->result[1] = s_am[n];
-    st->result[2] = new_len;
-    st->result[3] = st->status;
+    if (reject) {
+      st->result[0] = -1;
+      st->result[1] = st->pending;
+      st->result[2] = new_len;
+      st->result[3] = st->status | ST_BAD_STATE;
+      st->state_err = 1;
+    } else {
+      st->pending = s_am[n];
+      st->result[0] = n;
+      st->result[1] = s_am[n];
+      st->result[2] = new_len;
+      st->result[3] = st->status;
+    }
   }
   const int row = n_kv_heads * head_dim;
   for (int l = cta; l < n_layers; l += G_ctas) {

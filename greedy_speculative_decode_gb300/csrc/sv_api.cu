@@ -57,10 +57,14 @@ struct sv_ctx {
   // pinned host staging
   int32_t* pin_in = nullptr;   // [cap_len, tokens...] per row block of one call
   size_t pin_in_len = 0;       // ints: max_seq + one cap_len slot per block of a full prefill
-  int32_t* pin_out = nullptr;  // result[4] + seq_len + status
+  SvState* pin_out = nullptr;  // read-back of the device state
   int* pin_bt = nullptr;       // block table mirror
+  // test hook: the residual stream of each step's rows after every layer
+  bf16* trace = nullptr;  // [n_layers + 1][rows][hidden]
+  int trace_rows = 0;
   // host-side sequence state
   int seq_len = 0;
+  int pending = -1;  // greedy token after the committed sequence (-1: not known)
   int n_alloc = 0;  // logical pages with a physical page
   int bt_len = 0;   // entries of the block table
   std::vector<int> free_pages;
@@ -68,6 +72,32 @@ struct sv_ctx {
   std::vector<GraphEntry> graphs;
   std::string err;
 };
+
+namespace sv {
+
+bool make_bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  // the driver's encoder, looked up once per process (thread-safe initialisation)
+  static const PFN_cuTensorMapEncodeTiled_v12000 enc = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace sv
 
 namespace {
 
@@ -90,33 +120,6 @@ int fail(sv_ctx* c, int code, const char* fmt, ...) {
       return fail(ctx, SV_E_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));        \
   } while (0)
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-// 2D bf16 tensor [rows, cols] row-major, box [box_rows, 64 cols], 128B swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int n_tiles, int map) {
@@ -129,7 +132,7 @@ int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int
     return fail(ctx, SV_E_INVAL, "weight of %d x %d is split over %d CTAs per tile (max %d)", rows, Kd,
                 d->max_seg, kLinMaxSeg);
   d->map_kind = map;
-  if (!make_map(&d->map, w, (uint64_t)rows, (uint64_t)Kd, 64))
+  if (!make_bf16_map(&d->map, w, (uint64_t)rows, (uint64_t)Kd, 64))
     return fail(ctx, SV_E_CUDA, "cuTensorMapEncodeTiled failed for a weight of %d x %d", rows, Kd);
   return SV_OK;
 }
@@ -266,7 +269,17 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   const sv_config& c = ctx->cfg;
   const int H = c.hidden, d = c.head_dim, Hkv = c.n_kv_heads;
   cudaStream_t s = ctx->stream;
-  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, s));
+  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, mode == MODE_VERIFY, s));
+  // the trace hook copies the residual stream between kernels: no programmatic
+  // dependent launch while it is on
+  const bool tracing = ctx->trace != nullptr && M <= ctx->trace_rows;
+  const bool pdl = ctx->use_pdl && !tracing;
+  auto trace_copy = [&](int entry) -> cudaError_t {
+    if (!tracing) return cudaSuccess;
+    return cudaMemcpyAsync(ctx->trace + (size_t)entry * M * H, ctx->x, (size_t)M * H * sizeof(bf16),
+                           cudaMemcpyDeviceToDevice, s);
+  };
+  CK(trace_copy(0));
   const int G = c.n_q_heads / Hkv;
   const int n_rb = (M + kAttnQ / G - 1) / (kAttnQ / G);
   const int attn_items_max = ctx->max_splits * Hkv * n_rb;  // attention work items at max_seq
@@ -293,28 +306,28 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   };
   for (int l = 0; l < c.n_layers; ++l) {
     LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
-    CK(run_linear(ctx, *ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_QKV, l)));
+    CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_QKV, l)));
     AttnParams ap = attn_params(ctx, l, M);
-    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, ctx->use_pdl));
-    CK(launch_attn_combine(ap, d, s, ctx->use_pdl));
+    CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, pdl));
+    CK(launch_attn_combine(ap, d, s, pdl));
     for (int w : {LIN_O, LIN_GU, LIN_DOWN}) {
       p = lin_params(ctx, w, l, M, mode, logits, &epi, &norm, &ld);
-      CK(run_linear(ctx, *ld, p, epi, norm, s, ctx->use_pdl, next_of(w, l)));
+      CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(w, l)));
     }
+    CK(trace_copy(l + 1));
   }
   if (head) {  // final RMSNorm + LM head + per-tile argmax
     LinParams p = lin_params(ctx, LIN_HEAD, 0, M, mode, logits, &epi, &norm, &ld);
-    CK(run_linear(ctx, *ld, p, epi, norm, s, ctx->use_pdl, next_of(LIN_HEAD, 0)));
+    CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_HEAD, 0)));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
-                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s,
-                   ctx->use_pdl));
+                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s, pdl));
   return SV_OK;
 }
 
 // Run one step: replay (capturing on first use) the graph of this shape.
 int run_step(sv_ctx* ctx, int M, int mode, float* logits) {
-  if (!ctx->use_graphs) return enqueue_step(ctx, M, mode, logits);
+  if (!ctx->use_graphs || ctx->trace) return enqueue_step(ctx, M, mode, logits);
   for (auto& g : ctx->graphs)
     if (g.M == M && g.mode == mode && g.logits == logits) {
       CK(cudaGraphLaunch(g.exec, ctx->stream));
@@ -410,15 +423,21 @@ int check_tokens(sv_ctx* ctx, const int32_t* t, int n) {
 }
 
 int finish_sync_step(sv_ctx* ctx, int32_t* result) {
-  CK(cudaMemcpyAsync(ctx->pin_out, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost,
+  CK(cudaMemcpyAsync(ctx->pin_out->result, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost,
                      ctx->stream));
   CK(cudaStreamSynchronize(ctx->stream));
-  memcpy(result, ctx->pin_out, 4 * sizeof(int32_t));
-  if (result[3] != 0)
+  memcpy(result, ctx->pin_out->result, 4 * sizeof(int32_t));
+  if (result[3] & ~ST_BAD_STATE)
     return fail(ctx, SV_E_CUDA, "a kernel reported status 0x%x (1 timeout, 2 bad page, 4 bad token)",
                 result[3]);
   ctx->seq_len = result[2];
   release_pages(ctx, ctx->seq_len);
+  if (result[3] & ST_BAD_STATE) {  // the host check below makes this unreachable; kept as a backstop
+    CK(cudaMemsetAsync(&ctx->st->state_err, 0, sizeof(int32_t), ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+    return fail(ctx, SV_E_STATE, "tokens[0] is not the pending greedy token; nothing was committed");
+  }
+  ctx->pending = result[1];
   return SV_OK;
 }
 
@@ -540,15 +559,15 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
   if (cudaMemset(ctx->ws_tc, 0xff, ws_words * sizeof(uint32_t)) != cudaSuccess) return bail(SV_E_CUDA);
-  if (!make_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
-      !make_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
-      !make_map(&ctx->xmap_x, ctx->x, kMaxK, H, kMaxK) || !make_map(&ctx->xmap_o, ctx->o, kMaxK, Hq * d, kMaxK) ||
-      !make_map(&ctx->xmap_a, ctx->a, kMaxK, c.ffn, kMaxK))
+  if (!make_bf16_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
+      !make_bf16_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
+      !make_bf16_map(&ctx->xmap_x, ctx->x, kMaxK, H, kMaxK) || !make_bf16_map(&ctx->xmap_o, ctx->o, kMaxK, Hq * d, kMaxK) ||
+      !make_bf16_map(&ctx->xmap_a, ctx->a, kMaxK, c.ffn, kMaxK))
     return bail(SV_E_CUDA);
   // a prefill of max_seq tokens stages every block [cap_len, tokens] side by side
   ctx->pin_in_len = (size_t)c.max_seq + (c.max_seq + kMaxK - 1) / kMaxK + kMaxK + 8;
   if (cudaMallocHost(&ctx->pin_in, sizeof(int32_t) * ctx->pin_in_len) != cudaSuccess ||
-      cudaMallocHost(&ctx->pin_out, sizeof(int32_t) * 8) != cudaSuccess ||
+      cudaMallocHost(&ctx->pin_out, sizeof(SvState)) != cudaSuccess ||
       cudaMallocHost(&ctx->pin_bt, sizeof(int) * (size_t)ctx->bt_len) != cudaSuccess)
     return bail(SV_E_NOMEM);
   for (int i = 0; i < ctx->bt_len; ++i) ctx->pin_bt[i] = -1;
@@ -557,6 +576,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
     return bail(SV_E_CUDA);
   for (int pg = c.max_pages - 1; pg >= 0; --pg) ctx->free_pages.push_back(pg);
   if (launch_rope_table(ctx->rope, c.max_seq, d, c.rope_theta, ctx->stream) != cudaSuccess ||
+      launch_set_len(ctx->st, 0, 0, -1, ctx->stream) != cudaSuccess ||
       cudaStreamSynchronize(ctx->stream) != cudaSuccess)
     return bail(SV_E_CUDA);
   *out = ctx;
@@ -585,6 +605,9 @@ int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev,
   if (ctx->seq_len + K > ctx->cfg.max_seq)
     return fail(ctx, SV_E_INVAL, "length %d + %d exceeds max_seq", ctx->seq_len, K);
   if ((rc = begin_call(ctx))) return rc;
+  if (ctx->pending >= 0 && tokens_host[0] != ctx->pending)
+    return fail(ctx, SV_E_STATE, "tokens[0] = %d is not the pending greedy token %d", tokens_host[0],
+                ctx->pending);
   if ((rc = ensure_pages(ctx, ctx->seq_len + K))) return rc;
   if ((rc = upload_tokens(ctx, tokens_host, K, 0))) return rc;
   if ((rc = run_step(ctx, K, MODE_VERIFY, logits_dev))) return rc;
@@ -650,7 +673,7 @@ int sv_reserve(sv_ctx* ctx, int len) {
   int rc;
   if ((rc = begin_call(ctx))) return rc;
   if ((rc = ensure_pages(ctx, len))) return rc;
-  CK(launch_set_len(ctx->st, ctx->seq_len, ctx->n_alloc * kPage, ctx->stream));
+  CK(launch_set_len(ctx->st, ctx->seq_len, ctx->n_alloc * kPage, kKeepPending, ctx->stream));
   CK(cudaStreamSynchronize(ctx->stream));
   return end_call(ctx);
 }
@@ -658,12 +681,20 @@ int sv_reserve(sv_ctx* ctx, int len) {
 int sv_sync(sv_ctx* ctx) {
   if (!ctx) return SV_E_INVAL;
   CK(cudaStreamSynchronize(ctx->stream));
-  CK(cudaMemcpy(ctx->pin_out, ctx->st, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost));
+  CK(cudaMemcpy(ctx->pin_out, ctx->st, sizeof(SvState), cudaMemcpyDeviceToHost));
   ctx->async_pending = false;
-  ctx->seq_len = ctx->pin_out[0];
-  if (ctx->pin_out[2] != 0)
+  ctx->seq_len = ctx->pin_out->seq_len;
+  ctx->pending = ctx->pin_out->pending;
+  if (ctx->pin_out->status != 0)
     return fail(ctx, SV_E_CUDA, "a kernel reported status 0x%x (1 timeout, 2 bad page, 4 bad token)",
-                ctx->pin_out[2]);
+                ctx->pin_out->status);
+  if (ctx->pin_out->state_err != 0) {
+    CK(cudaMemsetAsync(&ctx->st->state_err, 0, sizeof(int32_t), ctx->stream));
+    CK(cudaStreamSynchronize(ctx->stream));
+    return fail(ctx, SV_E_STATE,
+                "an asynchronous verify step had tokens[0] != the pending greedy token; that step "
+                "committed nothing");
+  }
   return SV_OK;
 }
 
@@ -676,9 +707,12 @@ int sv_truncate(sv_ctx* ctx, int new_len) {
   const sv_config& c = ctx->cfg;
   CK(launch_kv_zero(ctx->kpool, ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers,
                     c.n_kv_heads, c.head_dim, new_len, ctx->seq_len, ctx->stream));
+  // a shorter sequence has no known greedy token until the next commit
+  const int pending = new_len == ctx->seq_len ? kKeepPending : -1;
+  if (pending == -1) ctx->pending = -1;
   ctx->seq_len = new_len;
   release_pages(ctx, new_len);
-  CK(launch_set_len(ctx->st, new_len, ctx->n_alloc * kPage, ctx->stream));
+  CK(launch_set_len(ctx->st, new_len, ctx->n_alloc * kPage, pending, ctx->stream));
   CK(cudaStreamSynchronize(ctx->stream));
   return end_call(ctx);
 }
@@ -688,16 +722,26 @@ int sv_seq_len(const sv_ctx* ctx) { return ctx ? ctx->seq_len : SV_E_INVAL; }
 int sv_kv_read(sv_ctx* ctx, int layer, int first, int count, void* k_dst_dev, void* v_dst_dev) {
   if (!ctx) return SV_E_INVAL;
   const sv_config& c = ctx->cfg;
-  if (layer < 0 || layer >= c.n_layers || first < 0 || count < 0 || first + count > ctx->seq_len ||
-      !k_dst_dev || !v_dst_dev)
-    return fail(ctx, SV_E_INVAL, "kv_read(layer %d, %d, %d) outside the sequence", layer, first, count);
   int rc;
   if ((rc = begin_call(ctx))) return rc;
+  if (layer < 0 || layer >= c.n_layers || first < 0 || count < 0 ||
+      first + count > ctx->n_alloc * kPage || !k_dst_dev || !v_dst_dev)
+    return fail(ctx, SV_E_INVAL, "kv_read(layer %d, %d, %d) outside the allocated pages (%d positions)",
+                layer, first, count, ctx->n_alloc * kPage);
   CK(launch_kv_gather(ctx->kpool, ctx->vpool, ctx->layer_stride, ctx->block_table, layer, c.n_kv_heads,
                       c.head_dim, first, count, static_cast<bf16*>(k_dst_dev), static_cast<bf16*>(v_dst_dev),
                       ctx->stream));
   CK(cudaStreamSynchronize(ctx->stream));
   return end_call(ctx);
+}
+
+int sv_trace_hidden(sv_ctx* ctx, void* hidden_dev, int max_rows) {
+  if (!ctx) return SV_E_INVAL;
+  if (hidden_dev && (max_rows < 1 || max_rows > kMaxK))
+    return fail(ctx, SV_E_INVAL, "trace of %d rows outside [1, %d]", max_rows, kMaxK);
+  ctx->trace = static_cast<bf16*>(hidden_dev);
+  ctx->trace_rows = hidden_dev ? max_rows : 0;
+  return SV_OK;
 }
 
 int sv_shuffle_pages(sv_ctx* ctx, uint64_t seed) {
@@ -740,8 +784,14 @@ int sv_spec_generate(sv_ctx* target, sv_ctx* draft, int32_t pending, int K, int 
   while (produced < n_new) {
     const int base = target->seq_len;  // == draft->seq_len
     block[0] = pending;
-    for (int j = 1; j < K; ++j)  // the drafter commits block[j - 1] and proposes block[j]
-      if ((rc = sv_decode(draft, block[j - 1], nullptr, &block[j])) != SV_OK) return drafter(rc);
+    // the drafter commits block[j - 1] and proposes block[j]: block[0] is the
+    // target's token, not the drafter's own greedy one, so it goes in as a
+    // one-token prefill; the later ones are the drafter's pending tokens
+    for (int j = 1; j < K; ++j) {
+      rc = j == 1 ? sv_prefill(draft, &block[0], 1, nullptr, &block[1])
+                  : sv_decode(draft, block[j - 1], nullptr, &block[j]);
+      if (rc != SV_OK) return drafter(rc);
+    }
     int32_t n = 0, corr = 0;
     if ((rc = sv_verify(target, block.data(), K, nullptr, &n, &corr)) != SV_OK) return rc;
     ++steps;

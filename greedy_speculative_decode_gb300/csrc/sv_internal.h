@@ -57,8 +57,11 @@ enum LinEpi : int { EPI_QKV = 0, EPI_RESID = 1, EPI_GLU = 2, EPI_LOGITS = 3 };
 enum LinMap : int { MAP_PLAIN = 0, MAP_GATE_UP = 1, MAP_HEAD256 = 2 };
 // Step kinds.
 enum StepMode : int { MODE_VERIFY = 0, MODE_PREFILL = 1, MODE_BODY = 2 };
-// Status bits a kernel can raise.
-enum Status : int { ST_TIMEOUT = 1, ST_BAD_PAGE = 2, ST_BAD_TOKEN = 4 };
+// Status bits a kernel can raise.  The first three are sticky (st->status):
+// the context is unusable after them.  ST_BAD_STATE is reported only in the
+// result of the step it concerns: tokens[0] of a verify step was not the
+// pending greedy token, so the step committed nothing.
+enum Status : int { ST_TIMEOUT = 1, ST_BAD_PAGE = 2, ST_BAD_TOKEN = 4, ST_BAD_STATE = 8 };
 
 // Device-resident state of the sequence and of the current step.
 // cap_len and tokens are adjacent so the host sets both with one copy.
@@ -70,6 +73,9 @@ struct SvState {
   int32_t tokens[kMaxK];
   int32_t result[4];  // n_accepted, correction, new_len, status
   int32_t argmax[kMaxK];
+  int32_t pending;      // greedy token after the committed sequence (-1: not known)
+  int32_t step_reject;  // this verify step's tokens[0] != pending (set by the embedding kernel)
+  int32_t state_err;    // a step was rejected since the host last looked (cleared by sv_sync)
 };
 
 struct LinParams {
@@ -140,8 +146,9 @@ size_t linear_smem_bytes(int mt);
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
                              int head_dim, int grid, bool multi, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_combine(const AttnParams& p, int head_dim, cudaStream_t s, bool pdl);
+// check: a verify step, whose tokens[0] must equal st->pending when that is known
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
-                         SvState* st, cudaStream_t s);
+                         SvState* st, bool check, cudaStream_t s);
 cudaError_t launch_accept(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                           int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                           const int* block_table, int n_layers, int n_kv_heads, int head_dim,
@@ -153,6 +160,11 @@ cudaError_t launch_kv_zero(bf16* kpool, bf16* vpool, size_t layer_stride, const 
 cudaError_t launch_kv_gather(const bf16* kpool, const bf16* vpool, size_t layer_stride,
                              const int* block_table, int layer, int n_kv_heads, int head_dim,
                              int first, int count, bf16* kdst, bf16* vdst, cudaStream_t s);
-cudaError_t launch_set_len(SvState* st, int len, int cap_len, cudaStream_t s);
+// pending: the new pending token, -1 for "not known", kKeepPending to leave it
+constexpr int kKeepPending = -2;
+cudaError_t launch_set_len(SvState* st, int len, int cap_len, int pending, cudaStream_t s);
+// 2D bf16 tensor map [rows, cols] row-major, boxes of box_rows x 64 columns,
+// 128B swizzle (the driver's encoder is looked up once per process).
+bool make_bf16_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 }  // namespace sv

@@ -10,12 +10,10 @@
 // buffers from sv_create; this one call needs none beyond its own inputs and
 // outputs.
 //
-// The split-K partial tiles, their tickets, the per-tile argmax partials, the
-// row sums of squares and the kernels' status word live in one file-scope
-// device array of kNoAllocScratchBytes.  Every GPU that loads the library
-// keeps that array until the process exits.
-#include <cudaTypedefs.h>
-
+// The split-tile partial slots (one per CTA, each value a tagged 64-bit word),
+// the per-tile argmax partials, the row sums of squares and the kernels'
+// status word live in one file-scope device array of kNoAllocScratchBytes.
+// Every GPU that loads the library keeps that array until the process exits.
 #include <mutex>
 
 #include "sv_internal.h"
@@ -138,13 +136,8 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   int* am_idx = reinterpret_cast<int*>(base + off_ami);
   unsigned long long* ws = reinterpret_cast<unsigned long long*>(base + off_ws);
 
-  // Tensor map of the weight: a host-side encoding, no device memory.
-  void* enc_fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &enc_fn, 12000, cudaEnableDefault, &q) !=
-          cudaSuccess ||
-      q != cudaDriverEntryPointSuccess)
-    return SV_E_CUDA;
+  // Tensor map of the weight: a host-side encoding (the driver's encoder is
+  // looked up once per process), no device memory.
   LinearDesc d;
   d.N = vocab;
   d.Kd = hidden;
@@ -152,17 +145,7 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   d.grid = grid;
   d.max_seg = max_seg;
   d.map_kind = MAP_PLAIN;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)hidden, (cuuint64_t)vocab};
-    cuuint64_t strides[1] = {(cuuint64_t)hidden * 2};
-    cuuint32_t box[2] = {64, 64};
-    cuuint32_t estr[2] = {1, 1};
-    if (reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(enc_fn)(
-            &d.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w_dev), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return SV_E_CUDA;
-  }
+  if (!make_bf16_map(&d.map, w_dev, (uint64_t)vocab, (uint64_t)hidden, 64)) return SV_E_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   // What must start at zero: the status word and the tags of the split-tile

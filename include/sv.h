@@ -26,9 +26,20 @@
  * pages hold it.  Logits are returned as fp32 holding bf16 values; argmax ties
  * go to the lowest token id.
  *
+ * The pending token: after every commit the library knows the target's
+ * greedy token after the committed sequence (sv_prefill's next_token,
+ * sv_decode's next_token, sv_verify's correction_token).  A verify window
+ * starts with it ("Phase 23" section 2: the window is the known-correct next
+ * token plus the drafts), so sv_verify and sv_decode reject any other
+ * tokens[0] with SV_E_STATE and change nothing.  Committing tokens the model
+ * did not choose (a prompt, forced ids) is sv_prefill's job.  After
+ * sv_truncate to a shorter length the pending token is not known, and the
+ * next window may start with any id.
+ *
  * Conventions for every call:
  *   - Return 0 (SV_OK) or a negative SV_E_* code; sv_last_error() then gives a
- *     message.  On SV_E_INVAL / SV_E_NOMEM the sequence state is unchanged.
+ *     message.  On SV_E_INVAL / SV_E_NOMEM / SV_E_STATE the sequence state is
+ *     unchanged.
  *     SV_E_CUDA means a CUDA call or a kernel's own bounds/timeout check
  *     failed; the context should then be destroyed.
  *   - Host pointers are read or written before the call returns; device
@@ -47,7 +58,8 @@ extern "C" {
 #define SV_E_INVAL (-1)       /* bad argument or unsupported shape */
 #define SV_E_NOMEM (-2)       /* page pool or device memory exhausted */
 #define SV_E_CUDA (-3)        /* CUDA error or a kernel reported a failed check */
-#define SV_E_STATE (-4)       /* call not valid in the current state */
+#define SV_E_STATE (-4)       /* call not valid in the current state (asynchronous work
+                                 pending, or tokens[0] not the pending greedy token) */
 
 #define SV_PAGE_SIZE 16       /* positions per KV page */
 #define SV_MAX_K 32           /* most rows in one verify / prefill block */
@@ -105,43 +117,62 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
 void sv_destroy(sv_ctx* ctx);
 
 /* Commit n tokens (host array) at positions len .. len+n-1, processed in
- * row blocks of up to 32 rows (whatever max_k is).  last_logits_dev: device fp32 [vocab] for
- * the logits after the last token, or NULL.  next_token: the greedy token
- * after the last one.  Synchronous. */
+ * row blocks of up to 32 rows (whatever max_k is).  last_logits_dev: device
+ * fp32 [vocab] for the logits after the last token, or NULL.  next_token: the
+ * greedy token after the last one (the new pending token).  Any ids may be
+ * committed.  The K/V of every position are bit-identical to those of
+ * one-token commits ("Shape and cache history in Gemma block verification",
+ * section "Same-prefix controls": one fresh prefill of the committed prefix is
+ * one of the three cache histories that must agree).  Synchronous. */
 int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logits_dev,
                int32_t* next_token);
 
-/* Commit one token and return the greedy next token; logits_dev [vocab] or
- * NULL.  Identical to sv_verify with K = 1.  Synchronous. */
+/* Commit the pending token and return the greedy next token; logits_dev
+ * [vocab] or NULL.  Identical to sv_verify with K = 1 (the single-token
+ * decode every verify row must equal: "Phase 23" section 2 step 3), including
+ * the SV_E_STATE check of `token`.  Synchronous. */
 int sv_decode(sv_ctx* ctx, int32_t token, float* logits_dev, int32_t* next_token);
 
 /* Block verify of K rows (host array) [pending, d_1 .. d_{K-1}] at positions
- * pos .. pos+K-1 (pos = current length).  Row 0 is always committed; drafts
- * are accepted while d_{j+1} equals the argmax of row j.  On return
- * n_accepted in [0, K-1], correction_token = argmax of row n_accepted, the
- * length is pos + 1 + n_accepted, and the K/V of rejected rows are zeroed.
- * logits_dev: device fp32 [K, vocab] or NULL.  Synchronous. */
+ * pos .. pos+K-1 (pos = current length): the window's K/V go into the cache
+ * in one shot and row r attends to pos+r+1 positions ("Phase 23" section 2
+ * steps 1-2).  Row 0 is always committed; drafts are accepted while d_{j+1}
+ * equals the argmax of row j (the greedy rule of the Gemma page, section
+ * "Mechanism and failure").  On return n_accepted in [0, K-1],
+ * correction_token = argmax of row n_accepted (the new pending token), the
+ * length is pos + 1 + n_accepted, and the K/V of rejected rows are zeroed
+ * ("Phase 23" section 2 steps 4-5).  tokens[0] must be the pending token
+ * when one is known (else SV_E_STATE, nothing changed).  logits_dev: device
+ * fp32 [K, vocab] or NULL.  Synchronous. */
 int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev,
               int32_t* n_accepted, int32_t* correction_token);
 
 /* Asynchronous verify with device-resident input and output, for callers that
- * keep drafts on the GPU.  tokens_dev: int32 [K]; result_dev: int32 [4] =
- * {n_accepted, correction_token, new_length, status (0 = ok)}.  The sequence
- * length is tracked on the device; pages must already cover every position
- * the call writes (see sv_reserve), otherwise the kernels skip the writes and
- * report a nonzero status.  Call sv_sync before any synchronous call. */
+ * keep drafts on the GPU (the same step as sv_verify).  tokens_dev: int32 [K];
+ * result_dev: int32 [4] = {n_accepted, correction_token, new_length, status
+ * (0 = ok)}.  The sequence length and pending token are tracked on the
+ * device; pages must already cover every position the call writes (see
+ * sv_reserve), otherwise the kernels skip the writes and report a nonzero
+ * status.  A step whose tokens[0] is not the pending token commits nothing:
+ * its result is {-1, pending, old length, status | 8}, and the next sv_sync
+ * returns SV_E_STATE.  Call sv_sync before any synchronous call. */
 int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits_dev,
                     int32_t* result_dev);
 
-/* Make pages cover positions [0, len).  Synchronous. */
+/* Make pages cover positions [0, len) (page-table bookkeeping of the paged
+ * cache that "Phase 23" section 2 step 1 writes into).  Synchronous. */
 int sv_reserve(sv_ctx* ctx, int len);
 
-/* Wait for asynchronous calls, read the device length back, release pages
- * beyond it, and report any kernel status error.  */
+/* Wait for asynchronous calls, read the device length and pending token back
+ * and report any kernel status error (SV_E_CUDA) or a rejected window
+ * (SV_E_STATE, see sv_verify_async).  Pages beyond the length are released
+ * by the next synchronous call that changes the length. */
 int sv_sync(sv_ctx* ctx);
 
 /* Roll the sequence back to new_len <= length: zero the K/V of the removed
- * positions and release their pages.  Synchronous. */
+ * positions and release their pages ("Phase 23" section 2 step 5: truncate
+ * the target cache to the accepted prefix).  A shorter length forgets the
+ * pending token.  Synchronous. */
 int sv_truncate(sv_ctx* ctx, int new_len);
 
 /* Greedy speculative generation: `draft` proposes, `target` verifies.
@@ -171,15 +202,28 @@ int sv_spec_generate(sv_ctx* target, sv_ctx* draft, int32_t pending, int K, int 
 /* Current committed length (as of the last synchronous call or sv_sync). */
 int sv_seq_len(const sv_ctx* ctx);
 
-/* Copy the cached K and V of positions [first, first+count) of one layer into
- * device buffers k_dst_dev, v_dst_dev, each bf16 [count, n_kv_heads, head_dim].
- * Positions must be < length.  Synchronous. */
+/* Test read of the paged cache ("Phase 23" section 2 step 1 is what writes
+ * it).  Copies the cached K and V of positions [first, first+count) of one
+ * layer into two device buffers k_dst_dev, v_dst_dev, each bf16 [count,
+ * n_kv_heads, head_dim].  Positions may run to the end of the last page the
+ * sequence holds, past its length: every slot there is zero (rejected rows
+ * and truncated positions are zeroed), which tests check.  Synchronous. */
 int sv_kv_read(sv_ctx* ctx, int layer, int first, int count, void* k_dst_dev, void* v_dst_dev);
 
 /* Shuffle the order in which free pages are handed out (seeded).  Results
  * must not depend on it; tests use it to build the same prefix on different
- * physical pages. */
+ * physical pages (a cache-history change in the sense of the Gemma page,
+ * section "Same-prefix controls"). */
 int sv_shuffle_pages(sv_ctx* ctx, uint64_t seed);
+
+/* Test hook for per-layer comparisons.  While hidden_dev is not NULL, every
+ * step of at most max_rows rows (1..32) also copies its residual stream into
+ * hidden_dev, bf16 [n_layers + 1][rows][hidden]: entry 0 holds the embedded
+ * rows, entry l + 1 the output of layer l (the last one is the input of the
+ * final RMSNorm).  Such steps run without CUDA graphs or programmatic
+ * dependent launch; results are bit-identical either way.  NULL turns it off.
+ * The buffer must stay valid while it is set. */
+int sv_trace_hidden(sv_ctx* ctx, void* hidden_dev, int max_rows);
 
 /* Number of kernel launches in one step of K rows, with (1) or without (0)
  * the LM head and acceptance. */
@@ -211,11 +255,16 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
  * Computes, for M rows x (bf16 [M, hidden], device):
  *   logits = bf16(RMSNorm(x; gain, eps) . W^T)   as fp32 [M, vocab] (device)
  *   argmax[m] = greedy token of row m (largest logit, lowest id on ties)
- * with the same batch-invariant linear kernel, K split and rounding as the
- * context's LM head; for a model with no layers its logits equal sv_verify's.
+ * with the same K split and rounding as the context's LM head.  It runs the
+ * mma.sync form of the batch-invariant linear for every M; the context runs
+ * that form up to 8 rows and the tcgen05 form for 9-32 rows, and the two are
+ * bit-identical, so for a model with no layers this call's logits and argmax
+ * equal sv_verify's bit for bit at every M.
  *   gain: bf16 [hidden]; W: bf16 [vocab, hidden]; all inputs 16-byte aligned.
  *   argmax_dev: int32 [M] or NULL; status_dev: int32 [1] or NULL, set to 0, or
- *     to the kernels' failure bits (1 timeout).
+ *     to the kernels' failure bits (1 timeout).  When the call returns non-zero,
+ *     logits_dev, argmax_dev and status_dev are undefined (work already queued
+ *     may or may not have written them).
  *   cuda_stream: the stream to run on (NULL = legacy stream).  Asynchronous.
  * Scratch: the split-K partials (one slot per CTA), the argmax partials and
  * the row statistics live in one fixed 8 MiB device array inside the library

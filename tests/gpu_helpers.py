@@ -63,6 +63,16 @@ def bits(t):
     return t.detach().contiguous().view(torch.uint8).cpu().numpy()
 
 
+def commit(ctx, tokens, pending):
+    """Commit ``tokens`` one at a time: a decode where the token is the
+    pending greedy token, else a one-token prefill (the library takes tokens
+    the model did not choose only through prefill).  Returns the new pending
+    token."""
+    for tok in tokens:
+        pending = ctx.decode(tok) if tok == pending else ctx.prefill([tok])
+    return pending
+
+
 def greedy_chain_gpu(ctx, prompt, n):
     """Prefill `prompt` then decode greedily; returns [t0, t1, ...] (n tokens),
     leaving ctx at len(prompt) + n - 1 committed tokens."""

@@ -105,18 +105,15 @@ def test_gemma_like_three_histories(gemma, K):
     committed = prompt + chain[:78]
     probe = chain[78:78 + K]
     a = gh.context(cfg, dw, max_k=16, max_seq=160, shuffle=1)
-    a.prefill(committed[:1])
-    for tok in committed[1:]:
-        a.decode(tok)
+    gh.commit(a, committed[1:], a.prefill(committed[:1]))
     b = gh.context(cfg, dw, max_k=16, max_seq=160, shuffle=2)
     b.prefill(prompt)
-    i = 0
+    i, pending = 0, None
     while len(b) + 8 <= len(committed):
-        n, _ = b.verify(chain[i:i + 8])
+        n, pending = b.verify(chain[i:i + 8])
         assert n == 7
         i += 8
-    for tok in committed[len(b):]:
-        b.decode(tok)
+    gh.commit(b, committed[len(b):], pending)
     c = gh.context(cfg, dw, max_k=16, max_seq=160, shuffle=3)
     c.prefill(committed)
     assert len(a) == len(b) == len(c) == len(committed) == 87

@@ -68,15 +68,21 @@ def test_concurrent_contexts_share_the_gpu(wide):
     waits only on CTAs dispatched before it)."""
     cfg, dw = wide
     prompts = [inputs.prefix_tokens(90 + i, 300 + 37 * i, cfg.vocab) for i in range(2)]
-    wins = [[[5 + j, 9, 13, 21][:4] for j in range(6)] for _ in range(2)]
+    # windows along each context's own greedy chain (drafts replaced with
+    # probability 0.5), so every window starts with the pending token that the
+    # previous asynchronous step leaves behind
+    wins = []
+    for i in range(2):
+        ref = gh.context(cfg, dw, max_k=8, max_seq=400)
+        chain = gh.greedy_chain_gpu(ref, prompts[i], 6 * 4 + 1)
+        ref.close()
+        wins.append([w for (_, w, _) in inputs.schedule(chain, 4, 6, seq=i, p=0.5, vocab=cfg.vocab)])
+        assert len(wins[i]) == 6
 
     def run(concurrent):
         ctxs = [gh.context(cfg, dw, max_k=8, max_seq=400, shuffle=i) for i in range(2)]
-        res, lgs = [], []
         for i, c in enumerate(ctxs):
-            t = c.prefill(prompts[i])
-            for w in wins[i]:
-                w[0] = t  # any committed token works; fix the same one for both runs
+            c.prefill(prompts[i])
             c.reserve(len(c) + 6 * 4)
         bufs = [[torch.zeros(4, dtype=torch.int32, device="cuda") for _ in range(6)] for _ in range(2)]
         logit = [[gh.logits_buf(4, cfg.vocab) for _ in range(6)] for _ in range(2)]

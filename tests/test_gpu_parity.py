@@ -140,19 +140,16 @@ def test_three_cache_histories_identical(tiny):
     probe = chain[78:78 + 8]         # a verify window after that prefix
     # (a) one-token commits
     a = gh.context(cfg, dw, max_k=16, max_seq=256, shuffle=1)
-    a.prefill(committed[:1])
-    for tok in committed[1:]:
-        a.decode(tok)
+    gh.commit(a, committed[1:], a.prefill(committed[:1]))
     # (b) accepted 8-row blocks: prompt, then K=8 all-accept verifies along the chain
     b = gh.context(cfg, dw, max_k=16, max_seq=256, shuffle=2)
     b.prefill(prompt)
-    i = 0
+    i, pending = 0, None
     while len(b) + 8 <= len(committed):
-        n, _ = b.verify(chain[i:i + 8])
+        n, pending = b.verify(chain[i:i + 8])
         assert n == 7
         i += 8
-    for tok in committed[len(b):]:
-        b.decode(tok)
+    gh.commit(b, committed[len(b):], pending)
     # (c) one fresh prefill
     c = gh.context(cfg, dw, max_k=16, max_seq=256, shuffle=3)
     c.prefill(committed)
@@ -244,10 +241,7 @@ def test_prefill_blocks_do_not_depend_on_max_k(tiny):
     cfg, hw, dw = tiny
     prompt = inputs.prefix_tokens(77, 100, cfg.vocab)
     ref = gh.context(cfg, dw, max_k=1, max_seq=128)
-    ref.prefill(prompt[:1])
-    for t in prompt[1:-1]:
-        ref.decode(t)
-    nxt = ref.decode(prompt[-1])
+    nxt = gh.commit(ref, prompt[1:], ref.prefill(prompt[:1]))
     for mk in (1, 4, 32):
         ctx = gh.context(cfg, dw, max_k=mk, max_seq=128, shuffle=mk)
         assert ctx.prefill(prompt) == nxt, mk

@@ -34,6 +34,19 @@ def test_binding_loads_and_names_the_same_calls():
         assert hasattr(sv.lib(), n)
 
 
+def test_no_alloc_binding_rejects_host_tensors():
+    """The allocation-free call takes device pointers: the binding refuses host
+    tensors before calling into the library."""
+    import torch
+    import greedy_speculative_decode_gb300 as sv
+    x = torch.zeros((2, 128), dtype=torch.bfloat16)
+    g = torch.ones((128,), dtype=torch.bfloat16)
+    w = torch.zeros((256, 128), dtype=torch.bfloat16)
+    lg = torch.empty((2, 256), dtype=torch.float32)
+    with pytest.raises(ValueError):
+        sv.lm_head_noalloc(x, g, w, lg)
+
+
 def _counters():
     out = {}
     for line in open(os.path.join(GOLDEN, "p2_bench_counters.txt")):
