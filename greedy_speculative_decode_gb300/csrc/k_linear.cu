@@ -135,6 +135,34 @@ size_t linear_smem_bytes(int mt) {
   return b;
 }
 
+namespace {
+
+// One 16-byte unit per thread-iteration: unit u of row r of chunk ch of block
+// blk (= tile * KB + kk) goes to granule u ^ (r mod 8) of that row.
+__global__ void k_tile_weight(const bf16* __restrict__ w, int N, int Kd, int n_tiles, int map_kind, int ffn,
+                              uint8_t* __restrict__ out) {
+  const int KB = Kd / kLinBK;
+  const size_t units = (size_t)n_tiles * KB * 1024;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < units; e += (size_t)gridDim.x * blockDim.x) {
+    const int u = (int)(e & 7), r = (int)((e >> 3) & 63), ch = (int)((e >> 9) & 1);
+    const size_t blk = e >> 10;
+    const int tile = (int)(blk / KB), kk = (int)(blk % KB);
+    const TileRows tr = tile_rows_of(map_kind, ffn, tile);
+    const int row = (ch == 0 ? tr.a0 : tr.b0) + r;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (row < N) v = __ldg(reinterpret_cast<const uint4*>(w + (size_t)row * Kd + kk * kLinBK + u * 8));
+    *reinterpret_cast<uint4*>(out + blk * kLinStageBytes + ch * kLinChunkBytes + r * 128 + ((u ^ (r & 7)) << 4)) = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tile_weight(const bf16* w, int N, int Kd, int n_tiles, int map_kind, int ffn, uint8_t* out,
+                               cudaStream_t s) {
+  k_tile_weight<<<1024, 256, 0, s>>>(w, N, Kd, n_tiles, map_kind, ffn, out);
+  return cudaGetLastError();
+}
+
 void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg) {
   const long long KB = Kd / kLinBK, T = (long long)n_tiles * KB;
   const long long by_share = T / kLinMinShare > 0 ? T / kLinMinShare : 1;
@@ -166,8 +194,10 @@ cudaError_t launch_linear(const LinearDesc& d, const LinParams& p_in, int epi, b
     p.pf_grid = next->grid;
     p.pf_map = next->map_kind;
     p.pf_ffn = next->N / 2;  // gate|up: the up rows start at ffn
+    p.pf_wt = next->tiled;
   } else {
     p.pf_blocks = 0;
+    p.pf_wt = nullptr;
   }
   const CUtensorMap& pf = next ? next->map : d.map;
   if (p.M <= 8) return launch_mt<1>(d, p, epi, norm, s, pdl, pf);

@@ -140,10 +140,7 @@ __device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CU
   if (n <= 0) return true;
   int tile = (int)(kb_begin / KB), kk = (int)(kb_begin % KB);
   auto weight = [&](int s) {
-    const TileRows tr = tile_rows(p, tile);
-    uint8_t* dst = sm.ring + s * kTcStageBytes;
-    tma_load_2d(dst, wmap, kk * kLinBK, tr.a0, &sm.full[s], pol_w);
-    tma_load_2d(dst + kLinChunkBytes, wmap, kk * kLinBK, tr.b0, &sm.full[s], pol_w);
+    load_weight_block(p, wmap, sm.ring + s * kTcStageBytes, tile, kk, &sm.full[s], pol_w);
   };
   auto input = [&](int s, int kcol) {
     tma_load_2d(sm.ring + s * kTcStageBytes + kLinStageBytes, xmap, kcol * kLinBK, 0, &sm.full[s], pol_x);

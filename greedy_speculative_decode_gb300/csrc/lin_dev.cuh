@@ -490,6 +490,22 @@ __device__ __forceinline__ void lin_range(const LinParams& p, int cta, int G, lo
   kb_end = (long long)(cta + 1) * Tk / G;
 }
 
+// One k-block (both 64-row chunks of `tile` at k-block kk) into `dst`,
+// completing on `bar`: one bulk copy from the tiled layout, else two box
+// loads from the row-major weight.  Either way the shared-memory bytes are
+// the same.
+__device__ __forceinline__ void load_weight_block(const LinParams& p, const CUtensorMap* wmap, uint8_t* dst,
+                                                  int tile, int kk, uint64_t* bar, uint64_t pol) {
+  if (p.wt != nullptr) {
+    const size_t blk = (size_t)tile * (p.Kd / kLinBK) + kk;
+    bulk_load_hint(dst, p.wt + blk * kLinStageBytes, kLinStageBytes, bar, pol);
+  } else {
+    const TileRows tr = tile_rows(p, tile);
+    tma_load_2d(dst, wmap, kk * kLinBK, tr.a0, bar, pol);
+    tma_load_2d(dst + kLinChunkBytes, wmap, kk * kLinBK, tr.b0, bar, pol);
+  }
+}
+
 // Producer (one thread): TMA the CTA's weight boxes into the ring.  `it`
 // counts ring uses (stage = it mod stages, parity = its quotient's low bit),
 // kept in step with the consumers'.  Returns false on a timeout.
@@ -503,11 +519,8 @@ __device__ bool lin_produce(const LinParams& p, const CUtensorMap* wmap, int cta
   for (long long kb = kb_begin; kb < kb_end; ++kb, ++it) {
     const int s = it % S;
     if (it >= S && !mbar_wait(&sm.empty[s], ((it / S) & 1) ^ 1)) return false;
-    const TileRows tr = tile_rows(p, tile);
     mbar_arrive_expect_tx(&sm.full[s], kLinStageBytes);
-    uint8_t* dst = sm.ring + s * kLinStageBytes;
-    tma_load_2d(dst, wmap, kk * kLinBK, tr.a0, &sm.full[s], pol);
-    tma_load_2d(dst + kLinChunkBytes, wmap, kk * kLinBK, tr.b0, &sm.full[s], pol);
+    load_weight_block(p, wmap, sm.ring + s * kLinStageBytes, tile, kk, &sm.full[s], pol);
     if (++kk == KB) {
       kk = 0;
       ++tile;
@@ -526,6 +539,10 @@ __device__ void lin_prefetch_next(const LinParams& p, const CUtensorMap* pfmap, 
   long long b1 = (long long)(cta + 1) * Tk / p.pf_grid;
   if (b1 > b0 + p.pf_blocks) b1 = b0 + p.pf_blocks;
   int tile = (int)(b0 / KB), kk = (int)(b0 % KB);
+  if (p.pf_wt != nullptr) {  // the tiled blocks are contiguous in this order
+    bulk_prefetch_l2(p.pf_wt + (size_t)b0 * kLinStageBytes, (uint32_t)((b1 - b0) * kLinStageBytes));
+    return;
+  }
   for (long long kb = b0; kb < b1; ++kb) {
     const TileRows tr = tile_rows_of(p.pf_map, p.pf_ffn, tile);
     tma_prefetch_l2(pfmap, kk * kLinBK, tr.a0);

@@ -30,6 +30,7 @@ struct sv_ctx {
   bool use_graphs = true;
   bool use_pdl = true;  // chain a step's kernels with programmatic dependent launch
   bool use_tc = true;   // 9-32 row linears on tcgen05 (bit-identical to the mma.sync form)
+  bool use_tiled = true;  // stream the linear weights from the context's tiled copy
   int prefetch_mode = 0;  // 0 none, 1 every linear prefetches the next one into L2, 2 only QKV -> O
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
@@ -134,6 +135,22 @@ int make_linear(sv_ctx* ctx, LinearDesc* d, const void* w, int rows, int Kd, int
   d->map_kind = map;
   if (!make_bf16_map(&d->map, w, (uint64_t)rows, (uint64_t)Kd, 64))
     return fail(ctx, SV_E_CUDA, "cuTensorMapEncodeTiled failed for a weight of %d x %d", rows, Kd);
+  d->tiled = nullptr;
+  if (ctx->use_tiled) {
+    // the context's own copy in the tiled layout: every k-block one
+    // contiguous 16 KB run, streamed with one bulk copy (every byte is
+    // written by the repack, so no clearing)
+    void* t = nullptr;
+    const size_t bytes = tiled_bytes(n_tiles, Kd);
+    cudaError_t e = cudaMalloc(&t, bytes);
+    if (e != cudaSuccess)
+      return fail(ctx, SV_E_NOMEM, "cudaMalloc(%zu) for a tiled weight failed: %s", bytes, cudaGetErrorString(e));
+    ctx->allocs.push_back(t);
+    d->tiled = static_cast<uint8_t*>(t);
+    e = launch_tile_weight(static_cast<const bf16*>(w), rows, Kd, n_tiles, map, map == MAP_GATE_UP ? rows / 2 : 0,
+                           d->tiled, ctx->stream);
+    if (e != cudaSuccess) return fail(ctx, SV_E_CUDA, "weight repack failed: %s", cudaGetErrorString(e));
+  }
   return SV_OK;
 }
 
@@ -241,6 +258,7 @@ LinParams lin_params(sv_ctx* ctx, int which, int l, int M, int mode, float* logi
   p.max_seg = ld->max_seg;
   p.map = ld->map_kind;
   p.grid = ld->grid;
+  p.wt = ld->tiled;
   *desc = ld;
   return p;
 }
@@ -491,9 +509,14 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   ctx->prefetch_mode = pf ? atoi(pf) : 0;
   const char* nt = getenv("SV_NO_TC");
   ctx->use_tc = !(nt && nt[0] == '1');
+  const char* nl = getenv("SV_NO_TILED");
+  ctx->use_tiled = !(nl && nl[0] == '1');
   if (prepare_linear_kernels() != cudaSuccess || prepare_linear_tc_kernels() != cudaSuccess ||
       prepare_attention_kernels() != cudaSuccess)
     return bail(SV_E_CUDA);
+  // the weights are read below (the tiled copies) on the library's stream:
+  // let every stream's earlier work, which may still be writing them, finish
+  if (cudaDeviceSynchronize() != cudaSuccess) return bail(SV_E_CUDA);
 
   const int L = c.n_layers, H = c.hidden, d = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   ctx->embed = static_cast<const bf16*>(w->embed);
@@ -872,7 +895,7 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
         ld = &ctx->lin_head; epi = EPI_LOGITS; norm = true; p.X = ctx->x; p.gain = ctx->final_norm;
       }
       p.Kd = ld->Kd; p.n_tiles = ld->n_tiles; p.max_seg = ld->max_seg; p.map = ld->map_kind;
-      p.grid = ld->grid;
+      p.grid = ld->grid; p.wt = ld->tiled;
       // the same class of the next layer is prefetched, as much as inside a step
       const LinearDesc* next = nullptr;
       if (ctx->prefetch_mode == 1 && which != SV_LIN_LM_HEAD) {

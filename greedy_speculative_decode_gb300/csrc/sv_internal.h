@@ -79,6 +79,10 @@ struct SvState {
 };
 
 struct LinParams {
+  // the weight in the tiled layout (see LinearDesc::tiled), or null: the
+  // producer then reads the row-major weight through the kernel's tensor map
+  const uint8_t* wt;
+  const uint8_t* pf_wt;  // the same for the weight of the L2 prefetch
   // input activations [M, Kd] bf16 and, for an RMSNorm prologue, the
   // per-128-column partial sums of squares of each row and the gain
   const bf16* X;
@@ -131,10 +135,22 @@ struct AttnParams {
 // ------------------------------------------------------------------ launches
 // A weight matrix as the linear kernel streams it: grid = one CTA per SM (at
 // most one per k-block), max_seg = most CTAs any 128-row tile is split over.
+// map: the row-major weight, 64 x 64 boxes.  tiled (or null): the same weight
+// as n_tiles x (Kd/64) blocks of kLinStageBytes, tile-major, each block the
+// exact shared-memory image of one k-block of one tile -- its two 64-row
+// chunks, each 64 rows x 128 bytes with the 16-byte units of row r at
+// positions u ^ (r mod 8) (the 128B swizzle the tensor map would apply) --
+// so one contiguous bulk copy replaces two strided box loads.
 struct LinearDesc {
   CUtensorMap map;
   int N, Kd, n_tiles, grid, max_seg, map_kind;
+  uint8_t* tiled = nullptr;
 };
+// Bytes of the tiled layout of a weight.
+inline size_t tiled_bytes(int n_tiles, int Kd) { return (size_t)n_tiles * (Kd / kLinBK) * kLinStageBytes; }
+// Write the tiled layout of a row-major bf16 weight [N, Kd] (rows past N are zero).
+cudaError_t launch_tile_weight(const bf16* w, int N, int Kd, int n_tiles, int map_kind, int ffn, uint8_t* out,
+                               cudaStream_t s);
 void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg);
 
 cudaError_t prepare_linear_kernels();

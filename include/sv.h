@@ -84,7 +84,11 @@ typedef struct {
 /* Device pointers to bf16 weights, row-major, borrowed for the context's
  * lifetime (the caller keeps them allocated and unchanged).  Each must be
  * 16-byte aligned.  Per-layer fields are HOST arrays of n_layers device
- * pointers (read during sv_create only).
+ * pointers (read during sv_create only).  sv_create also copies every linear
+ * weight (wqkv, wo, w_gate_up, w_down, the LM head) into a tiled layout the
+ * context owns and streams from: each 64-column k-block of a 128-row tile one
+ * contiguous 16 KB run (the same memory again, 15.1 GB for the 8B shape);
+ * SV_NO_TILED=1 streams the borrowed row-major weights instead.
  *   embed, lm_head [vocab, hidden] (lm_head may equal embed); final_norm [hidden]
  *   attn_norm, ffn_norm [hidden]; q_norm, k_norm [head_dim] (ignored if !qk_norm)
  *   wqkv [(n_q_heads + 2 n_kv_heads) head_dim, hidden]: q heads, k heads, v heads
@@ -101,7 +105,9 @@ typedef struct {
  * stream (cudaStream_t) or NULL for the legacy stream; the library orders its
  * own internal stream after it at the start of each call and the caller's
  * stream after the library's work at the end.  Allocates the KV pool, block
- * table, activations and workspaces (all owned by the context).
+ * table, activations, workspaces and the tiled weight copies (all owned by
+ * the context); it synchronises the device first, since it reads the
+ * weights.
  *
  * Environment switches, read here (results are bit-identical whichever are
  * set; they change only how the work is launched):
@@ -110,6 +116,8 @@ typedef struct {
  *   SV_NO_GRAPHS=1    launch every step's kernels directly instead of through
  *                     a CUDA graph per (rows, mode, logits buffer);
  *   SV_NO_PDL=1       no programmatic dependent launch between a step's kernels;
+ *   SV_NO_TILED=1     no tiled weight copies: the linears read the borrowed
+ *                     row-major weights (less memory, slower streaming);
  *   SV_L2_PREFETCH=n  1: each linear prefetches the next one's first k-blocks
  *                     into L2; 2: only the QKV linear does, for the attention
  *                     projection (off by default: it measured slower). */

@@ -107,3 +107,28 @@ def test_concurrent_contexts_share_the_gpu(wide):
     for i in range(2):
         for s in range(6):
             assert torch.equal(lseq[i][s], lcon[i][s]), (i, s)
+
+
+@pytest.mark.parametrize("K", [4, 17])
+def test_tiled_and_row_major_weights_give_identical_bits(wide, monkeypatch, K):
+    """The context's tiled weight copies hold the same shared-memory image of
+    every k-block as the row-major weights read through the tensor map, so a
+    step streamed from either gives the same logits and K/V, byte for byte
+    (K = 4: the mma.sync linear; K = 17: the tcgen05 one)."""
+    cfg, dw = wide
+    prompt = inputs.prefix_tokens(97, 200, cfg.vocab)
+    outs = []
+    for flag in ("0", "1"):
+        monkeypatch.setenv("SV_NO_TILED", flag)
+        ctx = gh.context(cfg, dw, max_k=32, max_seq=260)
+        t = ctx.prefill(prompt)
+        lg = gh.logits_buf(K, cfg.vocab)
+        ctx.verify([t] + [(7 * j + 3) % cfg.vocab for j in range(1, K)], logits=lg)
+        kv = [ctx.kv_read(layer, 0, len(ctx)) for layer in range(cfg.n_layers)]
+        outs.append((t, lg, kv))
+        ctx.close()
+    assert outs[0][0] == outs[1][0]
+    assert torch.equal(outs[0][1], outs[1][1])
+    for (ka, va), (kb, vb) in zip(outs[0][2], outs[1][2]):
+        assert torch.equal(ka.view(torch.int16), kb.view(torch.int16))
+        assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
