@@ -3,8 +3,8 @@
 // Row r of a step attends to positions [0, pos + r + 1) ("Phase 23:
 // Speculative Verify Parity" section 2 step 2: one metadata row per draft
 // token with context length pos+1 upward).  Work is split over absolute
-// positions: split s covers [256 s, 256 s + 256) and warp w of the CTA a fixed
-// run of its 16-position pages (two pages per warp for head_dim <= 128, four
+// positions: split s covers [128 s, 128 s + 128) and warp w of the CTA a fixed
+// run of its 16-position pages (one page per warp for head_dim <= 128, two
 // for 256).  Because these boundaries are
 // absolute, the partial result a row gets from a split does not depend on how
 // many other rows share the step, on the cache's history, or on its physical
@@ -42,9 +42,9 @@ struct AttnCfg {
   static constexpr int kQTileBytes = 16 * kQStride * 2;
   // warp-merge scratch: o rows of stride kOS floats (kOS = 8 mod 32 banks, so a
   // warp's float2 stores and float4 loads take the minimum two wavefronts),
-  // then the (m, l) pairs
+  // then the (m, l) pairs, the per-(query, warp) scales and the query maxima
   static constexpr int kOS = D + 8;
-  static constexpr int kScratchBytes = kWarps * 16 * kOS * 4 + kWarps * 16 * 8;
+  static constexpr int kScratchBytes = kWarps * 16 * kOS * 4 + kWarps * 16 * 8 + 16 * kWarps * 4 + 16 * 4;
 };
 
 // Shared memory of the attention work: per-warp page buffers, the warp-merge
@@ -78,6 +78,77 @@ template <int D, bool kMulti>
 __device__ __forceinline__ void attn_init_bars(const AttnSmem<D, kMulti>& sm) {
   for (int i = 0; i < AttnCfg<D>::kWarps * AttnCfg<D>::kBufs; ++i) mbar_init(&sm.bars[i], 1);
   fence_barrier_init();
+}
+
+// The item's warps' partials merged in warp order into the split partial
+// (m, l, o) of each of its nrows * G queries, written to global memory.  Each
+// (query, warp) scale exp2(m_w - m) is computed once, then every 8-column
+// group of a query takes the same ordered sums.  Named barrier 2; the caller
+// has synchronised the warps' use of `scratch` before.
+template <int D>
+__device__ __forceinline__ void attn_merge_warps(const AttnParams& p, float* scratch, int nrows, int G, int r0,
+                                                 int h, int split, const float (&m_run)[2], const float (&l_run)[2],
+                                                 const float (&o)[D / 8][4]) {
+  using C = AttnCfg<D>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q4 = lane & 3;
+  // scratch: o [warp][16][kOS], (m, l) [warp][16], scale [16][warp], max [16]
+  float* so = scratch;
+  float2* sml = reinterpret_cast<float2*>(scratch + C::kWarps * 16 * C::kOS);
+  float* s_sc = reinterpret_cast<float*>(sml + C::kWarps * 16);
+  float* s_mx = s_sc + 16 * C::kWarps;
+  if (q4 == 0) {
+    sml[warp * 16 + g] = make_float2(m_run[0], l_run[0]);
+    sml[warp * 16 + g + 8] = make_float2(m_run[1], l_run[1]);
+  }
+  {
+    float* r0p = so + (warp * 16 + g) * C::kOS + 2 * q4;
+    float* r1p = r0p + 8 * C::kOS;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      *reinterpret_cast<float2*>(r0p + n * 8) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(r1p + n * 8) = make_float2(o[n][2], o[n][3]);
+    }
+  }
+  named_sync(2, C::kThreads);
+  const int nq = nrows * G;
+  // the query's maximum over the warps, and each warp's scale against it
+  // (-1: the warp saw none of the query's positions and is skipped)
+  for (int e = tid; e < nq * C::kWarps; e += C::kThreads) {
+    const int qi = e / C::kWarps, ww = e % C::kWarps;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < C::kWarps; ++w2) mx = fmaxf(mx, sml[w2 * 16 + qi].x);
+    const float mw = sml[ww * 16 + qi].x;
+    s_sc[qi * C::kWarps + ww] = (mx == -INFINITY || mw == -INFINITY) ? -1.0f : exp2f(__fsub_rn(mw, mx));
+    if (ww == 0) s_mx[qi] = mx;
+  }
+  named_sync(2, C::kThreads);
+  // ordered sums over the warps, 8 columns per thread
+  for (int e = tid; e < nq * (D / 8); e += C::kThreads) {
+    const int qi = e / (D / 8), c0 = (e % (D / 8)) * 8;
+    float L = 0.0f, acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < C::kWarps; ++ww) {
+      const float sc = s_sc[qi * C::kWarps + ww];
+      if (sc < 0.0f) continue;
+      const float* src = so + (ww * 16 + qi) * C::kOS + c0;
+      const float4 v0 = *reinterpret_cast<const float4*>(src);
+      const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
+      const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      if (c0 == 0) L = __fadd_rn(L, __fmul_rn(sml[ww * 16 + qi].y, sc));
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(vv[c], sc));
+    }
+    const int r = r0 + qi / G, hq = h * G + qi % G;
+    const size_t slot = ((size_t)r * p.n_q_heads + hq) * p.max_splits + split;
+    if (c0 == 0) p.part_ml[slot] = make_float2(s_mx[qi], L);
+    float* dst = p.part_o + slot * D + c0;
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
 }
 
 // Work items w = cta, cta + G_ctas, ... of this step's attention, run by
@@ -126,7 +197,7 @@ __device__ bool attn_items_single(const AttnParams& p, const CUtensorMap* kmap_p
     const int nrows = min(RB, M - r0);
     const int ctx_max = pos + r0 + nrows;  // largest context of the block's rows
 
-    // ---- this warp's four pages
+    // ---- this warp's pages of the split
     const int wpos0 = split * kAttnSplit + warp * (C::kPagesPerWarp * kPage);
     int npages = 0;
     while (npages < C::kPagesPerWarp && wpos0 + npages * kPage < ctx_max) ++npages;
@@ -287,58 +358,7 @@ __device__ bool attn_items_single(const AttnParams& p, const CUtensorMap* kmap_p
     if (!ok) all_ok = false;
     named_sync(2, C::kThreads);  // every warp is done with its ring: reuse it as scratch
 
-    // ---- per-warp partials to scratch: o [warp][16][kOS], (m, l) [warp][16]
-    float* so = scratch;
-    float2* sml = reinterpret_cast<float2*>(scratch + C::kWarps * 16 * C::kOS);
-    if (q4 == 0) {
-      sml[warp * 16 + g] = make_float2(m_run[0], l_run[0]);
-      sml[warp * 16 + g + 8] = make_float2(m_run[1], l_run[1]);
-    }
-    {
-      float* r0p = so + (warp * 16 + g) * C::kOS + 2 * q4;
-      float* r1p = r0p + 8 * C::kOS;
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        *reinterpret_cast<float2*>(r0p + n * 8) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(r1p + n * 8) = make_float2(o[n][2], o[n][3]);
-      }
-    }
-    named_sync(2, C::kThreads);
-    // ---- merge the warps in order 0..3 and write the split partial
-    const int nq = nrows * G;
-    for (int e = tid; e < nq * (D / 8); e += C::kThreads) {
-      const int qi = e / (D / 8), c0 = (e % (D / 8)) * 8;
-      float2 mlw[C::kWarps];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < C::kWarps; ++ww) {
-        mlw[ww] = sml[ww * 16 + qi];
-        mx = fmaxf(mx, mlw[ww].x);
-      }
-      float L = 0.0f, acc[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
-      if (mx != -INFINITY) {
-#pragma unroll
-        for (int ww = 0; ww < C::kWarps; ++ww) {
-          if (mlw[ww].x == -INFINITY) continue;
-          const float sc = exp2f(__fsub_rn(mlw[ww].x, mx));
-          const float* src = so + (ww * 16 + qi) * C::kOS + c0;
-          const float4 v0 = *reinterpret_cast<const float4*>(src);
-          const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
-          const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-          L = __fadd_rn(L, __fmul_rn(mlw[ww].y, sc));
-#pragma unroll
-          for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(vv[c], sc));
-        }
-      }
-      const int r = r0 + qi / G, hq = h * G + qi % G;
-      const size_t slot = ((size_t)r * p.n_q_heads + hq) * p.max_splits + split;
-      if (c0 == 0) p.part_ml[slot] = make_float2(mx, L);
-      float* dst = p.part_o + slot * D + c0;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
+    attn_merge_warps<D>(p, scratch, nrows, G, r0, h, split, m_run, l_run, o);
     fence_proxy_async_smem();  // scratch (in the ring) is overwritten by TMA next item
     named_sync(2, C::kThreads);            // scratch (= ring) and Qs are rewritten by the next item
   }
@@ -609,58 +629,7 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
     }
     if (!ok) all_ok = false;
 
-    // ---- per-warp partials to scratch: o [warp][16][kOS], (m, l) [warp][16]
-    float* so = scratch;
-    float2* sml = reinterpret_cast<float2*>(scratch + C::kWarps * 16 * C::kOS);
-    if (q4 == 0) {
-      sml[warp * 16 + g] = make_float2(m_run[0], l_run[0]);
-      sml[warp * 16 + g + 8] = make_float2(m_run[1], l_run[1]);
-    }
-    {
-      float* r0p = so + (warp * 16 + g) * C::kOS + 2 * q4;
-      float* r1p = r0p + 8 * C::kOS;
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        *reinterpret_cast<float2*>(r0p + n * 8) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(r1p + n * 8) = make_float2(o[n][2], o[n][3]);
-      }
-    }
-    named_sync(2, C::kThreads);
-    // ---- merge the warps in order 0..3 and write the split partial
-    const int nq = nrows * G;
-    for (int e = tid; e < nq * (D / 8); e += C::kThreads) {
-      const int qi = e / (D / 8), c0 = (e % (D / 8)) * 8;
-      float2 mlw[C::kWarps];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < C::kWarps; ++ww) {
-        mlw[ww] = sml[ww * 16 + qi];
-        mx = fmaxf(mx, mlw[ww].x);
-      }
-      float L = 0.0f, acc[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) acc[c] = 0.0f;
-      if (mx != -INFINITY) {
-#pragma unroll
-        for (int ww = 0; ww < C::kWarps; ++ww) {
-          if (mlw[ww].x == -INFINITY) continue;
-          const float sc = exp2f(__fsub_rn(mlw[ww].x, mx));
-          const float* src = so + (ww * 16 + qi) * C::kOS + c0;
-          const float4 v0 = *reinterpret_cast<const float4*>(src);
-          const float4 v1 = *reinterpret_cast<const float4*>(src + 4);
-          const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-          L = __fadd_rn(L, __fmul_rn(mlw[ww].y, sc));
-#pragma unroll
-          for (int c = 0; c < 8; ++c) acc[c] = __fadd_rn(acc[c], __fmul_rn(vv[c], sc));
-        }
-      }
-      const int r = r0 + qi / G, hq = h * G + qi % G;
-      const size_t slot = ((size_t)r * p.n_q_heads + hq) * p.max_splits + split;
-      if (c0 == 0) p.part_ml[slot] = make_float2(mx, L);
-      float* dst = p.part_o + slot * D + c0;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
+    attn_merge_warps<D>(p, scratch, nrows, G, r0, h, split, m_run, l_run, o);
     if (has_next) {  // the next item's Q tile, into the other buffer
       bf16* Qn = sm.Qs + (qb ^ 1) * 16 * C::kQStride;
       for (int k = 0; k < kQV; ++k) {
@@ -681,12 +650,13 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
 }
 
 // One element of the split merge: out[r, hq, i] from the split partials s <
-// ceil((pos + r + 1) / 256), merged in order.  The partials of up to eight
-// splits (contexts up to 2048) are requested together; longer contexts take
-// the maximum in a first pass and accumulate in a second, eight at a time.
+// ceil((pos + r + 1) / kAttnSplit), merged in order.  The partials of up to
+// kCombineChunk splits (contexts up to 2048) are requested together; longer
+// contexts take the maximum in a first pass and accumulate in a second,
+// kCombineChunk at a time.
 template <int D>
 __device__ __forceinline__ void combine_element(const AttnParams& p, int r, int hq, int i, int pos) {
-  constexpr int kChunk = 8;
+  constexpr int kChunk = kCombineChunk;
   const int ctx = pos + r + 1;
   const int ns = (ctx + kAttnSplit - 1) / kAttnSplit;
   const size_t base = ((size_t)r * p.n_q_heads + hq) * p.max_splits;

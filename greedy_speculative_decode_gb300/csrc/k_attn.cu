@@ -3,8 +3,8 @@
 // Row r of a step attends to positions [0, pos + r + 1) ("Phase 23:
 // Speculative Verify Parity" section 2 step 2: one metadata row per draft
 // token with context length pos+1 upward).  Work is split over absolute
-// positions: split s covers [256 s, 256 s + 256) and warp w of the CTA a fixed
-// run of its 16-position pages (two pages per warp for head_dim <= 128, four
+// positions: split s covers [128 s, 128 s + 128) and warp w of the CTA a fixed
+// run of its 16-position pages (one page per warp for head_dim <= 128, two
 // for 256).  Because these boundaries are
 // absolute, the partial result a row gets from a split does not depend on how
 // many other rows share the step, on the cache's history, or on its physical
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
 }
 
 // One block per (row, query head), one thread per element.  Contexts of at
-// most eight splits use this light form (few registers, so its blocks fit
+// most kCombineChunk splits use this light form (few registers, so its blocks fit
 // beside the attention kernel's and are resident before it ends).
 template <int D>
 __global__ void __launch_bounds__(D) k_attn_combine(const AttnParams p) {
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(D) k_attn_combine(const AttnParams p) {
                      __ldcg(&p.st->step_pos));
 }
 
-// Longer contexts: rows of more than eight splits take combine_long.
+// Longer contexts: rows of more than kCombineChunk splits take combine_long.
 // Dynamic shared memory: the (m, l) pairs of up to max_splits splits.
 // (Its register cap lets its blocks fit beside an attention block.)
 template <int D>
@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(D, 768 / D) k_attn_combine_long(const AttnPara
   const int r = blockIdx.x / p.n_q_heads, hq = blockIdx.x % p.n_q_heads;
   const int pos = __ldcg(&p.st->step_pos);
   const int ns = (pos + r + kAttnSplit) / kAttnSplit;  // splits row r sees
-  if (ns <= 8)
+  if (ns <= kCombineChunk)
     combine_element<D>(p, r, hq, threadIdx.x, pos);
   else
     combine_long<D>(p, r, hq, ns, s_ml, s_red);
@@ -107,7 +107,7 @@ cudaError_t launch_comb_t(const AttnParams& p, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.M * p.n_q_heads);
   cfg.blockDim = dim3(D);
-  const bool long_ctx = p.max_splits > 8;
+  const bool long_ctx = p.max_splits > kCombineChunk;
   cfg.dynamicSmemBytes = long_ctx ? (size_t)p.max_splits * sizeof(float2) : 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -122,8 +122,12 @@ cudaError_t launch_comb_t(const AttnParams& p, cudaStream_t s, bool pdl) {
 
 template <int D, bool kMulti>
 cudaError_t prepare_attn_t() {
-  return cudaFuncSetAttribute(k_attention<D, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              AttnSmem<D, kMulti>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_attention<D, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       AttnSmem<D, kMulti>::kSmem);
+  if (e != cudaSuccess || kMulti) return e;
+  // the staged merge's (m, l) pairs: up to kMaxSeq / kAttnSplit splits
+  return cudaFuncSetAttribute(k_attn_combine_long<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)((kMaxSeq / kAttnSplit) * sizeof(float2)));
 }
 
 }  // namespace

@@ -44,10 +44,14 @@ constexpr int kLinPrefetchBlocks = 16;
 constexpr int kLinConsumerWarps = 8;
 constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;  // consumers, then the TMA producer
 
-// Attention geometry: a split is 256 absolute positions = 4 warps x 4 pages.
-constexpr int kAttnSplit = 256;  // positions per split (split s: [256 s, 256 s + 256))
-// Longest sequence a context may hold: the split merge stages the (m, l)
-// pairs of every split in shared memory (8 bytes each, 32 KB at this bound).
+// Attention geometry: a split is 128 absolute positions (8 warps x 1 page for
+// head_dim <= 128, 4 warps x 2 pages for 256).
+constexpr int kAttnSplit = 128;  // positions per split (split s: [128 s, 128 s + 128))
+// Splits whose partials the light merge requests in one round (contexts up
+// to 2048 positions); longer rows take the staged merge.
+constexpr int kCombineChunk = 16;
+// Longest sequence a context may hold: the staged split merge keeps the
+// (m, l) pairs of every split in shared memory (8 bytes each, 64 KB here).
 constexpr int kMaxSeq = 1 << 20;
 constexpr int kAttnQ = 16;  // query rows (token rows x heads of one group) per work item
 
