@@ -764,11 +764,14 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
       // word with tag 1 in its high half.  The stores are the message: no
       // fence, no ticket, and nothing waits here.
       unsigned long long* slot = p.ws + (size_t)cta * kLinRows * MP;
+      const bool withheld = cta == p.withhold_cta1 - 1;  // test hook (see LinParams)
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const int m0 = t * 8 + 2 * q;
-        st_relaxed_v2_u64(slot + lr0 * MP + m0, tagged(acc[t][0]), tagged(acc[t][1]));
-        st_relaxed_v2_u64(slot + (lr0 + 8) * MP + m0, tagged(acc[t][2]), tagged(acc[t][3]));
+        if (!withheld) {
+          st_relaxed_v2_u64(slot + lr0 * MP + m0, tagged(acc[t][0]), tagged(acc[t][1]));
+          st_relaxed_v2_u64(slot + (lr0 + 8) * MP + m0, tagged(acc[t][2]), tagged(acc[t][3]));
+        }
         acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
       }
       continue;

@@ -32,6 +32,7 @@ struct sv_ctx {
   bool use_tc = true;   // 9-32 row linears on tcgen05 (bit-identical to the mma.sync form)
   bool use_tiled = true;  // stream the linear weights from the context's tiled copy
   int prefetch_mode = 0;  // 0 none, 1 every linear prefetches the next one into L2, 2 only QKV -> O
+  int withhold_cta1 = 0;  // test hook: see LinParams::withhold_cta1 (first linear of a step only)
   // weights
   const bf16 *embed = nullptr, *lm_head = nullptr, *final_norm = nullptr;
   std::vector<const bf16*> attn_norm, q_norm, k_norm, ffn_norm;
@@ -324,6 +325,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   };
   for (int l = 0; l < c.n_layers; ++l) {
     LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
+    if (l == 0) p.withhold_cta1 = ctx->withhold_cta1;
     CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_QKV, l)));
     AttnParams ap = attn_params(ctx, l, M);
     CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, pdl));
@@ -511,6 +513,8 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   ctx->use_tc = !(nt && nt[0] == '1');
   const char* nl = getenv("SV_NO_TILED");
   ctx->use_tiled = !(nl && nl[0] == '1');
+  const char* wh = getenv("SV_TEST_WITHHOLD_PARTIAL");
+  ctx->withhold_cta1 = wh ? atoi(wh) + 1 : 0;
   if (prepare_linear_kernels() != cudaSuccess || prepare_linear_tc_kernels() != cudaSuccess ||
       prepare_attention_kernels() != cudaSuccess)
     return bail(SV_E_CUDA);

@@ -122,6 +122,10 @@ struct LinParams {
   // next linear of the step (that weight's tensor map is the kernel's second
   // parameter), so the next launch starts from L2 instead of a cold HBM ramp.
   int pf_blocks, pf_n_tiles, pf_Kd, pf_grid, pf_map, pf_ffn;
+  // Failure-detection test hook: CTA (withhold_cta1 - 1) never hands over its
+  // split-tile partial, so the tile's reducer polls a tag that nothing sets
+  // until its bounded wait gives up (0: off, the zero-initialised default).
+  int withhold_cta1;
 };
 
 struct AttnParams {

@@ -110,7 +110,7 @@ typedef struct {
  * weights.
  *
  * Environment switches, read here (results are bit-identical whichever are
- * set; they change only how the work is launched):
+ * set, the last one excepted; they change only how the work is launched):
  *   SV_NO_TC=1        steps of 9..32 rows use the mma.sync linear instead of
  *                     the tcgen05 one;
  *   SV_NO_GRAPHS=1    launch every step's kernels directly instead of through
@@ -120,7 +120,14 @@ typedef struct {
  *                     row-major weights (less memory, slower streaming);
  *   SV_L2_PREFETCH=n  1: each linear prefetches the next one's first k-blocks
  *                     into L2; 2: only the QKV linear does, for the attention
- *                     projection (off by default: it measured slower). */
+ *                     projection (off by default: it measured slower);
+ *   SV_TEST_WITHHOLD_PARTIAL=c  failure-detection test only: in the first
+ *                     linear of every step (steps of at most 8 rows), CTA c
+ *                     never hands its split-tile partial to the CTA that
+ *                     finishes the tile, whose bounded wait (2 s) then gives
+ *                     up: the call returns SV_E_CUDA (status bit 1, timeout)
+ *                     and the context must be destroyed.  Results are then
+ *                     wrong; never set it otherwise. */
 int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_ctx** out);
 void sv_destroy(sv_ctx* ctx);
 

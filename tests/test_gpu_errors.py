@@ -126,3 +126,31 @@ def test_bad_configurations_are_rejected(tiny):
     with pytest.raises(sv.SvError) as e:
         sv.Context(cfg, dw, max_k=33, max_seq=64)  # more rows than a step holds (32)
     assert e.value.code == sv.SV_E_INVAL
+
+
+def test_a_partial_that_never_arrives_times_out_and_a_new_context_works(monkeypatch):
+    """Failure detection without a fault: with the test switch, one CTA of the
+    step's first linear withholds its split-tile partial, so the tile's
+    reducer polls a tag that nothing sets.  Its wait is bounded (2 s): the
+    kernel gives up, raises the timeout bit and returns, the call reports
+    SV_E_CUDA, and the device stays usable -- a new context computes what a
+    context that never saw the switch computes."""
+    sv = _codes()
+    cfg = inputs.shrink(inputs.QWEN3_8B, n_layers=1, vocab=8192)  # split tiles in the QKV linear
+    _, dw = gh.make(cfg, seed=0, gain_std=0.1, host=False)
+    prompt = inputs.prefix_tokens(73, 6, cfg.vocab)
+    ref = gh.context(cfg, dw, max_k=8, max_seq=64)
+    t_ref = ref.prefill(prompt)
+    lg_ref = gh.logits_buf(4, cfg.vocab)
+    ref.verify([t_ref, 1, 2, 3], logits=lg_ref)
+    monkeypatch.setenv("SV_TEST_WITHHOLD_PARTIAL", "1")
+    bad = gh.context(cfg, dw, max_k=8, max_seq=64)
+    msg = _expect(sv.SV_E_CUDA, bad.prefill, prompt)
+    assert "status 0x1" in msg and "timeout" in msg
+    bad.close()
+    monkeypatch.delenv("SV_TEST_WITHHOLD_PARTIAL")
+    fresh = gh.context(cfg, dw, max_k=8, max_seq=64)
+    assert fresh.prefill(prompt) == t_ref
+    lg = gh.logits_buf(4, cfg.vocab)
+    fresh.verify([t_ref, 1, 2, 3], logits=lg)
+    assert torch.equal(lg, lg_ref)
