@@ -61,6 +61,10 @@ def parse():
                     help="time the draft -> verify loop against plain decoding (separate JSON line)")
     ap.add_argument("--prefill", action="store_true",
                     help="time sv_prefill of --prefix tokens (separate JSON line)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="long-context stress: prefixes 4096 and 32768, K in 1, 2, 4, 8, 16, forced "
+                         "all-accept / reject at slot 0 / reject at slot K/2 (one JSON line per point)")
+    ap.add_argument("--sweep-steps", type=int, default=256, help="verify steps per sweep point")
     ap.add_argument("--linear-only", action="store_true",
                     help="time each linear class once per layer (NVTX range 'linear') and exit")
     return ap.parse_args()
@@ -460,10 +464,90 @@ def run_prefill(args):
                       "hbm_frac": streamed / best / 1e9 / hbm_peak}))
 
 
+def run_sweep(args):
+    """The long-context stress workload: for each prefix length and K, the
+    three forced acceptance patterns, each a run of --sweep-steps verify steps
+    along the target's own greedy chain (every window starts with the pending
+    token the previous step left), timed with CUDA events on the caller's
+    stream with the windows already on the device.  Every step's acceptance,
+    correction and new length are checked against the chain."""
+    import torch
+
+    import greedy_speculative_decode_gb300 as sv
+    cfg = model_config(args)
+    hbm_peak, peak_kind = peaks()
+    stream = torch.cuda.current_stream()
+    weights = inputs.device_weights(cfg, seed=0, gain_std=0.0)
+    Ks, S = (1, 2, 4, 8, 16), args.sweep_steps
+    patterns = (("all-accept", None), ("reject-slot-0", 0), ("reject-slot-K/2", "mid"))
+    clocks = ClockSampler(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    for prefix in (4096, 32768):
+        n_chain = S * max(Ks) + max(Ks) + 1
+        max_seq = prefix + n_chain + 32
+        ctx = sv.Context(cfg, weights, max_k=max(Ks), max_seq=max_seq, stream=stream)
+        prompt = inputs.prefix_tokens(60 + prefix % 7, prefix, cfg.vocab)
+        t = ctx.prefill(prompt)
+        chain = [t]
+        for _ in range(n_chain - 1):
+            t = ctx.decode(t)
+            chain.append(t)
+        logits = torch.empty((max(Ks), cfg.vocab), dtype=torch.float32, device="cuda")
+        for K in Ks:
+            for name, rej in patterns:
+                reject_at = K // 2 if rej == "mid" else rej
+                if reject_at is not None and reject_at >= K - 1:
+                    continue  # no such draft slot at this K (or it is the all-accept run again)
+                ctx.sync()
+                ctx.truncate(prefix)  # releases the pages past the prefix: reserve them again
+                ctx.reserve(max_seq)
+                wins, i = [], 0
+                for _ in range(S):
+                    toks, n_exp = inputs.window(chain, i, K, vocab=cfg.vocab, reject_at=reject_at)
+                    wins.append((i, toks, n_exp))
+                    i += n_exp + 1
+                win = torch.tensor([w[1] for w in wins], dtype=torch.int32, device="cuda")
+                res = torch.zeros((S, 4), dtype=torch.int32, device="cuda")
+                for j in range(3):  # warm-up: the same shape's graph, then back to the prefix
+                    ctx.verify_async(win[j], K, res[j], logits)
+                ctx.sync()
+                ctx.truncate(prefix)
+                ctx.reserve(max_seq)
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(S + 1)]
+                torch.cuda.synchronize()
+                ev[0].record(stream)
+                for j in range(S):
+                    ctx.verify_async(win[j], K, res[j], logits)
+                    ev[j + 1].record(stream)
+                torch.cuda.synchronize()
+                ctx.sync()
+                step_ms = [ev[j].elapsed_time(ev[j + 1]) for j in range(S)]
+                total_ms = ev[0].elapsed_time(ev[S])
+                r = res.cpu().tolist()
+                bad = sum(1 for (i0, toks, n_exp), (n, corr, new_len, st) in zip(wins, r)
+                          if n != n_exp or corr != chain[i0 + n + 1] or st != 0 or new_len != prefix + i0 + n + 1)
+                tokens = sum(n + 1 for n, _, _, _ in r)
+                mean_pos = prefix + sum(w[0] for w in wins) / S
+                sb = step_bytes(cfg, K, mean_pos)
+                print(json.dumps({
+                    "mode": "sweep", "config": cfg.name, "prefix": prefix, "K": K, "pattern": name,
+                    "steps": S, "verify_step_us": {"median": 1000 * statistics.median(step_ms),
+                                                   "p90": 1000 * sorted(step_ms)[int(0.9 * (S - 1))],
+                                                   "mean": 1000 * total_ms / S},
+                    "tok_s": tokens / (total_ms / 1000.0), "tokens_per_step": tokens / S,
+                    "acceptance_rate": sum(n for n, _, _, _ in r) / max(1, S * (K - 1)),
+                    "step_bytes": sb, "hbm_frac_step": sb / (total_ms / S / 1000.0) / 1e9 / hbm_peak,
+                    "peak_gbs": hbm_peak, "peak_kind": peak_kind, "mismatches": bad}), flush=True)
+        ctx.close()
+    print(json.dumps({"mode": "sweep-clocks", "clocks": clocks.stop()}))
+
+
 def run_ours(args):
     import torch
 
     import greedy_speculative_decode_gb300 as sv
+    if args.sweep:
+        return run_sweep(args)
     if args.linear_only:
         return run_linear_only(args)
     if args.spec:

@@ -3,9 +3,9 @@
 // Row r of a step attends to positions [0, pos + r + 1) ("Phase 23:
 // Speculative Verify Parity" section 2 step 2: one metadata row per draft
 // token with context length pos+1 upward).  Work is split over absolute
-// positions: split s covers [128 s, 128 s + 128) and warp w of the CTA a fixed
-// run of its 16-position pages (one page per warp for head_dim <= 128, two
-// for 256).  Because these boundaries are
+// positions (attn_split_start: 128-position splits up to position 2048, then
+// 4 pages per warp) and warp w of the CTA takes a fixed run of the split's
+// 16-position pages.  Because these boundaries are
 // absolute, the partial result a row gets from a split does not depend on how
 // many other rows share the step, on the cache's history, or on its physical
 // pages; positions a row may not see are masked to exact zeros.  Partials are
@@ -29,14 +29,14 @@ namespace {
 
 template <int D>
 struct AttnCfg {
-  // warps per CTA, each over kPagesPerWarp consecutive 16-position pages of the split
-  static constexpr int kWarps = D <= 128 ? 8 : 4;
-  static constexpr int kPagesPerWarp = kAttnSplit / kPage / kWarps;
+  // warps per CTA, each over up to kMaxPages consecutive 16-position pages of a split
+  static constexpr int kWarps = attn_warps(D);
+  static constexpr int kMaxPages = kAttnPagesB;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kBoxes = D / 64;                // 64-column boxes per page row
   static constexpr int kPageBytes = kPage * D * 2;     // one K (or V) page of one head
   static constexpr int kBufBytes = 2 * kPageBytes;     // K + V
-  static constexpr int kBufs = kPagesPerWarp < 2 ? kPagesPerWarp : 2;  // pages in flight per warp
+  static constexpr int kBufs = 2;  // pages in flight per warp
   static constexpr int kQStride = D + 8;               // bf16 elements
   static constexpr int kRingBytes = kWarps * kBufs * kBufBytes;
   static constexpr int kQTileBytes = 16 * kQStride * 2;
@@ -177,7 +177,7 @@ __device__ bool attn_items_single(const AttnParams& p, const CUtensorMap* kmap_p
   const int RB = kAttnQ / G;  // token rows per work item
   const int M = p.M;
   const int n_rb = (M + RB - 1) / RB;
-  const int n_splits = (pos + M + kAttnSplit - 1) / kAttnSplit;
+  const int n_splits = attn_n_splits(pos + M, D);
   const int work = n_splits * p.n_kv_heads * n_rb;
   uint64_t* my_bars = bars + warp * C::kBufs;
   uint8_t* my_ring = ring + warp * C::kBufs * C::kBufBytes;
@@ -198,11 +198,12 @@ __device__ bool attn_items_single(const AttnParams& p, const CUtensorMap* kmap_p
     const int ctx_max = pos + r0 + nrows;  // largest context of the block's rows
 
     // ---- this warp's pages of the split
-    const int wpos0 = split * kAttnSplit + warp * (C::kPagesPerWarp * kPage);
+    const int ppw = attn_split_pages(split, D);
+    const int wpos0 = attn_split_start(split, D) + warp * (ppw * kPage);
     int npages = 0;
-    while (npages < C::kPagesPerWarp && wpos0 + npages * kPage < ctx_max) ++npages;
-    int page_id[C::kPagesPerWarp];
-    for (int j = 0; j < C::kPagesPerWarp; ++j) {
+    while (npages < ppw && wpos0 + npages * kPage < ctx_max) ++npages;
+    int page_id[C::kMaxPages];
+    for (int j = 0; j < C::kMaxPages; ++j) {
       int pg = -1;
       if (j < npages) {
         const int lp = (wpos0 + j * kPage) / kPage;
@@ -388,7 +389,7 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
   const int RB = kAttnQ / G;  // token rows per work item
   const int M = p.M;
   const int n_rb = (M + RB - 1) / RB;
-  const int n_splits = (pos + M + kAttnSplit - 1) / kAttnSplit;
+  const int n_splits = attn_n_splits(pos + M, D);
   const int work = n_splits * p.n_kv_heads * n_rb;
   uint64_t* my_bars = bars + warp * C::kBufs;
   uint8_t* my_ring = ring + warp * C::kBufs * C::kBufBytes;
@@ -404,7 +405,7 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
   // on an invalid block-table entry).
   struct Pages {
     int h, wpos0, npages;
-    int page_id[C::kPagesPerWarp];
+    int page_id[C::kMaxPages];
   };
   auto pages_of = [&](int w) {
     Pages pg;
@@ -412,12 +413,13 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
     pg.h = (w / n_rb) % p.n_kv_heads;
     const int split = w / (n_rb * p.n_kv_heads);
     const int ctx_max = pos + min(rb * RB + RB, M);  // largest context of the block's rows
-    pg.wpos0 = split * kAttnSplit + warp * (C::kPagesPerWarp * kPage);
+    const int ppw = attn_split_pages(split, D);
+    pg.wpos0 = attn_split_start(split, D) + warp * (ppw * kPage);
     pg.npages = 0;
-    while (pg.npages < C::kPagesPerWarp && pg.wpos0 + pg.npages * kPage < ctx_max) ++pg.npages;
+    while (pg.npages < ppw && pg.wpos0 + pg.npages * kPage < ctx_max) ++pg.npages;
     bool bad = false;
 #pragma unroll
-    for (int j = 0; j < C::kPagesPerWarp; ++j) {
+    for (int j = 0; j < C::kMaxPages; ++j) {
       int id = -1;
       if (j < pg.npages) {
         id = p.block_table[(pg.wpos0 + j * kPage) / kPage];
@@ -442,7 +444,7 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
     mbar_arrive_expect_tx(&my_bars[b], C::kBufBytes);
     int id = pg.page_id[0];  // select with constant indices: the ids stay in registers
 #pragma unroll
-    for (int t = 1; t < C::kPagesPerWarp; ++t)
+    for (int t = 1; t < C::kMaxPages; ++t)
       if (j == t) id = pg.page_id[t];
     const int row0 = ((layer * max_pages + id) * p.n_kv_heads + pg.h) * kPage;
     for (int cb = 0; cb < C::kBoxes; ++cb) {
@@ -649,8 +651,8 @@ __device__ bool attn_items_multi(const AttnParams& p, const CUtensorMap* kmap_p,
   return all_ok;
 }
 
-// One element of the split merge: out[r, hq, i] from the split partials s <
-// ceil((pos + r + 1) / kAttnSplit), merged in order.  The partials of up to
+// One element of the split merge: out[r, hq, i] from the partials of the
+// splits that cover [0, pos + r + 1), merged in order.  The partials of up to
 // kCombineChunk splits (contexts up to 2048) are requested together; longer
 // contexts take the maximum in a first pass and accumulate in a second,
 // kCombineChunk at a time.
@@ -658,7 +660,7 @@ template <int D>
 __device__ __forceinline__ void combine_element(const AttnParams& p, int r, int hq, int i, int pos) {
   constexpr int kChunk = kCombineChunk;
   const int ctx = pos + r + 1;
-  const int ns = (ctx + kAttnSplit - 1) / kAttnSplit;
+  const int ns = attn_n_splits(ctx, D);
   const size_t base = ((size_t)r * p.n_q_heads + hq) * p.max_splits;
   float2 ml[kChunk];
   float ov[kChunk];

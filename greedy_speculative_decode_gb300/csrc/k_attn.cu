@@ -3,9 +3,9 @@
 // Row r of a step attends to positions [0, pos + r + 1) ("Phase 23:
 // Speculative Verify Parity" section 2 step 2: one metadata row per draft
 // token with context length pos+1 upward).  Work is split over absolute
-// positions: split s covers [128 s, 128 s + 128) and warp w of the CTA a fixed
-// run of its 16-position pages (one page per warp for head_dim <= 128, two
-// for 256).  Because these boundaries are
+// positions (attn_split_start: 128-position splits up to position 2048, then
+// 4 pages per warp) and warp w of the CTA takes a fixed run of the split's
+// 16-position pages.  Because these boundaries are
 // absolute, the partial result a row gets from a split does not depend on how
 // many other rows share the step, on the cache's history, or on its physical
 // pages; positions a row may not see are masked to exact zeros.  Partials are
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(D, 768 / D) k_attn_combine_long(const AttnPara
   pdl_wait();
   const int r = blockIdx.x / p.n_q_heads, hq = blockIdx.x % p.n_q_heads;
   const int pos = __ldcg(&p.st->step_pos);
-  const int ns = (pos + r + kAttnSplit) / kAttnSplit;  // splits row r sees
+  const int ns = attn_n_splits(pos + r + 1, D);  // splits row r sees
   if (ns <= kCombineChunk)
     combine_element<D>(p, r, hq, threadIdx.x, pos);
   else
@@ -125,9 +125,9 @@ cudaError_t prepare_attn_t() {
   cudaError_t e = cudaFuncSetAttribute(k_attention<D, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        AttnSmem<D, kMulti>::kSmem);
   if (e != cudaSuccess || kMulti) return e;
-  // the staged merge's (m, l) pairs: up to kMaxSeq / kAttnSplit splits
+  // the staged merge's (m, l) pairs: up to the splits of kMaxSeq positions
   return cudaFuncSetAttribute(k_attn_combine_long<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)((kMaxSeq / kAttnSplit) * sizeof(float2)));
+                              (int)(attn_n_splits(kMaxSeq, D) * sizeof(float2)));
 }
 
 }  // namespace

@@ -559,7 +559,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   ctx->bt_len = pages_for(c.max_seq);
   ctx->layer_stride = (size_t)c.max_pages * Hkv * kPage * d;
   const size_t pool = ctx->layer_stride * (L > 0 ? L : 1);
-  ctx->max_splits = (c.max_seq + kAttnSplit - 1) / kAttnSplit;
+  ctx->max_splits = attn_n_splits(c.max_seq, d);
   size_t ws_words = 0;
   auto acc_ws = [&](const LinearDesc& ld) {
     if (ld.max_seg > 1) ws_words = std::max(ws_words, (size_t)ld.grid * kLinRows * MP);

@@ -44,14 +44,36 @@ constexpr int kLinPrefetchBlocks = 16;
 constexpr int kLinConsumerWarps = 8;
 constexpr int kLinThreads = (kLinConsumerWarps + 1) * 32;  // consumers, then the TMA producer
 
-// Attention geometry: a split is 128 absolute positions (8 warps x 1 page for
-// head_dim <= 128, 4 warps x 2 pages for 256).
-constexpr int kAttnSplit = 128;  // positions per split (split s: [128 s, 128 s + 128))
-// Splits whose partials the light merge requests in one round (contexts up
-// to 2048 positions); longer rows take the staged merge.
-constexpr int kCombineChunk = 16;
-// Longest sequence a context may hold: the staged split merge keeps the
-// (m, l) pairs of every split in shared memory (8 bytes each, 64 KB here).
+// Attention geometry.  Splits are fixed ranges of absolute positions: 128
+// positions each below position 2048 (one page per warp for head_dim <= 128,
+// whose CTAs have 8 warps; two for 256, 4 warps), then four pages per warp
+// (512 positions, or 256 for head_dim 256).  Short contexts get many short
+// dependent chains; long ones fewer work items, each merging more positions.
+constexpr int kAttnSplitA = 128;                           // split size below kAttnRegionA
+constexpr int kAttnRegionA = 2048;
+constexpr int kAttnSplitsA = kAttnRegionA / kAttnSplitA;   // 16
+constexpr int kAttnPagesB = 4;                             // pages per warp beyond kAttnRegionA
+__host__ __device__ constexpr int attn_warps(int head_dim) { return head_dim <= 128 ? 8 : 4; }
+__host__ __device__ constexpr int attn_split_b(int head_dim) { return kAttnPagesB * 16 * attn_warps(head_dim); }
+// Splits that cover positions [0, ctx).
+__host__ __device__ inline int attn_n_splits(int ctx, int head_dim) {
+  if (ctx <= kAttnRegionA) return (ctx + kAttnSplitA - 1) / kAttnSplitA;
+  const int sb = attn_split_b(head_dim);
+  return kAttnSplitsA + (ctx - kAttnRegionA + sb - 1) / sb;
+}
+// First position of split s, and pages per warp in it.
+__host__ __device__ inline int attn_split_start(int s, int head_dim) {
+  return s < kAttnSplitsA ? s * kAttnSplitA : kAttnRegionA + (s - kAttnSplitsA) * attn_split_b(head_dim);
+}
+__host__ __device__ inline int attn_split_pages(int s, int head_dim) {
+  return s < kAttnSplitsA ? kAttnSplitA / 16 / attn_warps(head_dim) : kAttnPagesB;
+}
+// Splits whose partials the light merge requests in one round: every row
+// whose context lies in the short-split region.  Longer rows take the staged
+// merge.
+constexpr int kCombineChunk = kAttnSplitsA;
+// Longest sequence a context may hold (the staged merge keeps the (m, l)
+// pairs of every split in shared memory: at most 33 KB).
 constexpr int kMaxSeq = 1 << 20;
 constexpr int kAttnQ = 16;  // query rows (token rows x heads of one group) per work item
 
