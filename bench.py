@@ -65,6 +65,8 @@ def parse():
                     help="long-context stress: prefixes 4096 and 32768, K in 1, 2, 4, 8, 16, forced "
                          "all-accept / reject at slot 0 / reject at slot K/2 (one JSON line per point)")
     ap.add_argument("--sweep-steps", type=int, default=256, help="verify steps per sweep point")
+    ap.add_argument("--kv-delayed", action="store_true",
+                    help="delayed K/V write-through: commit a window's K/V after acceptance")
     ap.add_argument("--linear-only", action="store_true",
                     help="time each linear class once per layer (NVTX range 'linear') and exit")
     return ap.parse_args()
@@ -485,7 +487,8 @@ def run_sweep(args):
     for prefix in (4096, 32768):
         n_chain = S * max(Ks) + max(Ks) + 1
         max_seq = prefix + n_chain + 32
-        ctx = sv.Context(cfg, weights, max_k=max(Ks), max_seq=max_seq, stream=stream)
+        ctx = sv.Context(cfg, weights, max_k=max(Ks), max_seq=max_seq, stream=stream,
+                         kv_delayed=args.kv_delayed)
         prompt = inputs.prefix_tokens(60 + prefix % 7, prefix, cfg.vocab)
         t = ctx.prefill(prompt)
         chain = [t]
@@ -531,6 +534,7 @@ def run_sweep(args):
                 sb = step_bytes(cfg, K, mean_pos)
                 print(json.dumps({
                     "mode": "sweep", "config": cfg.name, "prefix": prefix, "K": K, "pattern": name,
+                    "kv_commit": "delayed write-through" if args.kv_delayed else "write-then-truncate",
                     "steps": S, "verify_step_us": {"median": 1000 * statistics.median(step_ms),
                                                    "p90": 1000 * sorted(step_ms)[int(0.9 * (S - 1))],
                                                    "mean": 1000 * total_ms / S},
@@ -571,7 +575,8 @@ def run_ours(args):
 
     weights = inputs.device_weights(cfg, seed=0, gain_std=0.0)
     max_seq = args.prefix + GEN_TOKENS + 2 * K + 16
-    make_ctx = lambda: sv.Context(cfg, weights, max_k=max(K, 32), max_seq=max_seq, stream=stream)
+    make_ctx = lambda: sv.Context(cfg, weights, max_k=max(K, 32), max_seq=max_seq, stream=stream,
+                                  kv_delayed=args.kv_delayed)
     seqs = build_sequences(make_ctx, cfg, K, W + S, args.prefix, args.p)
     steps = [(sq, i, toks, n_exp) for sq in seqs for (i, toks, n_exp) in sq["sched"]]
     assert len(steps) >= W + S
@@ -660,6 +665,7 @@ def run_ours(args):
                                f"{GEN_TOKENS} generated tokens per sequence, draft slots corrupted "
                                f"with p={args.p}",
                    "K": K, "prefix": args.prefix, "sequences": len(seqs),
+                   "kv_commit": "delayed write-through" if args.kv_delayed else "write-then-truncate",
                    "l2": f"inputs larger than L2: {cfg.weight_bytes() / 1e9:.2f} GB of weights "
                          f"streamed per step", "parallelism": "replicas"},
         "verify_step_us": {"median": 1000 * statistics.median(step_ms),

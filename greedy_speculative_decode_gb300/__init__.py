@@ -29,7 +29,7 @@ class SvConfig(ctypes.Structure):
                                    "ffn", "vocab")] + [
         ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)] + [
         (n, _i32) for n in ("qk_norm", "act", "tie_embeddings", "page_size", "max_pages", "max_k",
-                            "max_seq")]
+                            "max_seq", "kv_delayed")]
 
 
 LAYER_KEYS = ("attn_norm", "wqkv", "q_norm", "k_norm", "wo", "ffn_norm", "w_gate_up", "w_down")
@@ -158,16 +158,18 @@ class Context:
     qk_norm, act, tie_embeddings). weights: mapping (name, layer) -> CUDA
     tensor of bf16 values (layer -1 for embed / lm_head / final_norm), the
     layout of include/sv.h; the tensors must outlive the context.
+    kv_delayed: commit a verify window's K/V only after acceptance (sv_config
+    kv_delayed = 1) instead of writing it and zeroing the rejected rows.
     """
 
     def __init__(self, cfg, weights, *, max_k: int, max_seq: int, max_pages: int | None = None,
-                 stream=None):
+                 stream=None, kv_delayed: bool = False):
         self.cfg = cfg
         self.max_k, self.max_seq = max_k, max_seq
         pages = max_pages if max_pages is not None else (max_seq + PAGE_SIZE - 1) // PAGE_SIZE
         self._c = SvConfig(cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
                            cfg.ffn, cfg.vocab, cfg.rms_eps, cfg.rope_theta, cfg.qk_norm, cfg.act,
-                           cfg.tie_embeddings, PAGE_SIZE, pages, max_k, max_seq)
+                           cfg.tie_embeddings, PAGE_SIZE, pages, max_k, max_seq, int(bool(kv_delayed)))
         self._weights = weights  # keep the tensors alive
         w = SvWeights()
         w.embed = _ptr(weights[("embed", -1)])

@@ -22,6 +22,10 @@ __global__ void __launch_bounds__(128) k_embed(const bf16* __restrict__ E, int h
     st->step_reject = (check && pending >= 0 && st->tokens[0] != pending) ? 1 : 0;
   }
   embed_tile(E, hidden, vocab, x, x_ss, ss_tiles, st, m, t, i, part, 3);
+  // Launched as a dependent of the delayed write-through window copy, which
+  // touches none of the above, this kernel ends only after the copy has: the
+  // step's later kernels wait for this one.  (No-op otherwise.)
+  pdl_wait();
 }
 
 // Acceptance for the whole step; CTA l zeroes the rejected rows of layer l.
@@ -29,13 +33,48 @@ __global__ void __launch_bounds__(256) k_accept(SvState* st, const float* __rest
                                                 const int* __restrict__ am_idx, int n_tiles, int M,
                                                 int mode, bf16* kpool, bf16* vpool,
                                                 size_t layer_stride, const int* block_table,
-                                                int n_layers, int n_kv_heads, int head_dim) {
+                                                int n_layers, int n_kv_heads, int head_dim, KvDelay dl) {
   pdl_trigger();
   pdl_wait();
   __shared__ int s_am[kMaxK];
   __shared__ int s_n;
   accept_work(st, am_val, am_idx, n_tiles, M, mode, kpool, vpool, layer_stride, block_table,
-              n_layers, n_kv_heads, head_dim, blockIdx.x, gridDim.x, s_am, &s_n);
+              n_layers, n_kv_heads, head_dim, dl, blockIdx.x, gridDim.x, s_am, &s_n);
+}
+
+// Delayed write-through: before a verify step of M rows at pos = seq_len,
+// map its window's logical pages (those that hold a physical page: below
+// cap_len) to the scratch pages in the shadow table and copy the real pages
+// there (positions past the length are zero in the real pages), 16 bytes per
+// thread-iteration.
+__global__ void k_kv_window_in(bf16* kpool, bf16* vpool, size_t layer_stride, const int* block_table,
+                               KvDelay dl, const SvState* st, int n_layers, int n_kv_heads, int head_dim,
+                               int M) {
+  pdl_trigger();  // the embedding gather runs beside the copy
+  const int pos = st->seq_len, cap = st->cap_len;
+  const int lp0 = pos / kPage;
+  const int lp_last = min(min(dl.bt_len, (cap + kPage - 1) / kPage) - 1, (pos + M - 1) / kPage);
+  const int npg = lp_last - lp0 + 1;  // at most kWinPages; none when the window has no page
+  if (npg <= 0) return;
+  if (blockIdx.x == 0 && (int)threadIdx.x < npg) dl.bt_shadow[lp0 + threadIdx.x] = dl.win0 + threadIdx.x;
+  const size_t pv = (size_t)n_kv_heads * kPage * head_dim / 8;  // 16-byte vectors per page
+  const size_t n = (size_t)n_layers * npg * pv;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+    const int l = (int)(e / (npg * pv));
+    const size_t r = e % (npg * pv);
+    const int t = (int)(r / pv);
+    const size_t w = r % pv;
+    const int real = block_table[lp0 + t];
+    uint4* kd = reinterpret_cast<uint4*>(kpool + (size_t)l * layer_stride) + (size_t)(dl.win0 + t) * pv + w;
+    uint4* vd = reinterpret_cast<uint4*>(vpool + (size_t)l * layer_stride) + (size_t)(dl.win0 + t) * pv + w;
+    uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+    if (real >= 0 && real < dl.win0) {
+      kv = reinterpret_cast<const uint4*>(kpool + (size_t)l * layer_stride)[(size_t)real * pv + w];
+      vv = reinterpret_cast<const uint4*>(vpool + (size_t)l * layer_stride)[(size_t)real * pv + w];
+    }
+    *kd = kv;
+    *vd = vv;
+  }
 }
 
 // cos/sin of pos * theta^(-2i/d), taken in double and rounded to fp32.
@@ -120,20 +159,29 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAtt
 }  // namespace
 
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
-                         SvState* st, bool check, cudaStream_t s) {
-  k_embed<<<dim3(hidden / 128, M), 128, 0, s>>>(E, hidden, vocab, x, x_ss, hidden / 128, st,
-                                                check ? 1 : 0);
-  return cudaGetLastError();
+                         SvState* st, bool check, cudaStream_t s, bool pdl) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = make_cfg(dim3(hidden / 128, M), dim3(128), s, attr, pdl);
+  return cudaLaunchKernelEx(&cfg, k_embed, E, hidden, vocab, x, x_ss, hidden / 128, st, check ? 1 : 0);
 }
 
 cudaError_t launch_accept(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                           int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                           const int* block_table, int n_layers, int n_kv_heads, int head_dim,
-                          cudaStream_t s, bool pdl) {
+                          const KvDelay& dl, cudaStream_t s, bool pdl) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n_layers > 0 ? n_layers : 1), dim3(256), s, attr, pdl);
   return cudaLaunchKernelEx(&cfg, k_accept, st, am_val, am_idx, n_tiles, M, mode, kpool, vpool,
-                            layer_stride, block_table, n_layers, n_kv_heads, head_dim);
+                            layer_stride, block_table, n_layers, n_kv_heads, head_dim, dl);
+}
+
+cudaError_t launch_kv_window_in(bf16* kpool, bf16* vpool, size_t layer_stride, const int* block_table,
+                                const KvDelay& dl, const SvState* st, int n_layers, int n_kv_heads,
+                                int head_dim, int M, cudaStream_t s) {
+  if (n_layers <= 0) return cudaSuccess;
+  k_kv_window_in<<<608, 256, 0, s>>>(kpool, vpool, layer_stride, block_table, dl, st, n_layers, n_kv_heads,
+                                      head_dim, M);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, float theta, cudaStream_t s) {

@@ -39,12 +39,15 @@ __device__ __forceinline__ void embed_tile(const bf16* __restrict__ E, int hidde
 // writes the results; the K/V of rejected rows are zeroed in layers
 // cta, cta + G_ctas, ...  A verify step whose tokens[0] was not the pending
 // greedy token (step_reject) commits no row: every row of it is zeroed and
-// the length and pending token stay as they were.  Runs on 256 threads
-// (named barrier 1).
+// the length and pending token stay as they were.  With delayed write-through
+// (dl.bt_shadow) a verify step's rows are in the scratch pages instead: the
+// accepted ones are copied into the real pages, nothing needs zeroing, and
+// the shadow table gets the real pages back.  Runs on 256 threads (named
+// barrier 1).
 __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                             int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                             const int* block_table, int n_layers, int n_kv_heads, int head_dim,
-                            int cta, int G_ctas, int* s_am, int* s_n) {
+                            const KvDelay& dl, int cta, int G_ctas, int* s_am, int* s_n) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pos = __ldcg(&st->step_pos);
   if (mode == MODE_BODY) {
@@ -57,16 +60,26 @@ __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx,
     }
     return;
   }
+  // Lane l takes tiles l, l + 32, ... in that order (so the result is the
+  // same however the loads are batched), eight loads in flight at a time.
   for (int r = warp; r < M; r += 8) {
     float best = -INFINITY;
     int bidx = 0x7fffffff;
-    for (int t = lane; t < n_tiles; t += 32) {
-      const float v = __ldcg(&am_val[r * n_tiles + t]);
-      const int id = __ldcg(&am_idx[r * n_tiles + t]);
-      if (bidx == 0x7fffffff || v > best || (v == best && id < bidx)) {
-        best = v;
-        bidx = id;
+    for (int t0 = lane; t0 < n_tiles; t0 += 32 * 8) {
+      float v[8];
+      int id[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = t0 + 32 * u;
+        v[u] = t < n_tiles ? __ldcg(&am_val[r * n_tiles + t]) : -INFINITY;
+        id[u] = t < n_tiles ? __ldcg(&am_idx[r * n_tiles + t]) : 0x7fffffff;
       }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (id[u] != 0x7fffffff && (bidx == 0x7fffffff || v[u] > best || (v[u] == best && id[u] < bidx))) {
+          best = v[u];
+          bidx = id[u];
+        }
     }
     for (int o = 1; o < 32; o <<= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, best, o);
@@ -108,17 +121,46 @@ __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx,
       st->result[3] = st->status;
     }
   }
-  const int row = n_kv_heads * head_dim;
+  // K/V rows move in 16-byte vectors: a row of one kv head is head_dim
+  // contiguous elements of its page.  Only positions below cap_len have pages.
+  const int cap = __ldcg(&st->cap_len);
+  const int vh = head_dim / 8;                   // vectors per (row, kv head)
+  const int vrow = n_kv_heads * vh;              // vectors per row
+  const size_t pv = (size_t)n_kv_heads * kPage * vh;  // vectors per page
+  auto vec_off = [&](int page, int ps, int u) {  // vector u of row ps in `page`
+    return (size_t)page * pv + ((size_t)(u / vh) * kPage + ps % kPage) * vh + u % vh;
+  };
+  if (dl.bt_shadow != nullptr && mode == MODE_VERIFY) {
+    const int lp0 = pos / kPage;
+    for (int l = cta; l < n_layers; l += G_ctas) {
+      uint4* kl = reinterpret_cast<uint4*>(kpool + (size_t)l * layer_stride);
+      uint4* vl = reinterpret_cast<uint4*>(vpool + (size_t)l * layer_stride);
+      for (int e = tid; e < (new_len - pos) * vrow; e += 256) {  // the accepted rows
+        const int ps = pos + e / vrow, u = e % vrow;
+        const int page = ps < cap ? block_table[ps / kPage] : -1;
+        if (page < 0) continue;
+        const size_t src = vec_off(dl.win0 + ps / kPage - lp0, ps, u), dst = vec_off(page, ps, u);
+        kl[dst] = kl[src];
+        vl[dst] = vl[src];
+      }
+    }
+    if (cta == 0 && tid < kWinPages) {
+      const int lp = lp0 + tid;
+      if (lp < dl.bt_len) dl.bt_shadow[lp] = block_table[lp];
+    }
+    return;
+  }
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   for (int l = cta; l < n_layers; l += G_ctas) {
-    for (int e = tid; e < (pos + M - new_len) * row; e += 256) {
-      const int ps = new_len + e / row, hi = e % row;
-      const int page = block_table[ps / kPage];
+    uint4* kl = reinterpret_cast<uint4*>(kpool + (size_t)l * layer_stride);
+    uint4* vl = reinterpret_cast<uint4*>(vpool + (size_t)l * layer_stride);
+    for (int e = tid; e < (pos + M - new_len) * vrow; e += 256) {  // the rejected rows
+      const int ps = new_len + e / vrow, u = e % vrow;
+      const int page = ps < cap ? block_table[ps / kPage] : -1;
       if (page < 0) continue;
-      const int h = hi / head_dim, i = hi % head_dim;
-      const size_t idx = (size_t)l * layer_stride +
-                         (((size_t)page * n_kv_heads + h) * kPage + ps % kPage) * head_dim + i;
-      kpool[idx] = __float2bfloat16_rn(0.0f);
-      vpool[idx] = __float2bfloat16_rn(0.0f);
+      const size_t idx = vec_off(page, ps, u);
+      kl[idx] = zero;
+      vl[idx] = zero;
     }
   }
 }

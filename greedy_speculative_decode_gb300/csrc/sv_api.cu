@@ -44,7 +44,9 @@ struct sv_ctx {
   std::vector<void*> allocs;
   bf16 *kpool = nullptr, *vpool = nullptr;
   size_t layer_stride = 0;  // elements per layer in each pool
+  int pool_pages = 0;       // pages per layer: max_pages, plus kWinPages scratch pages when delayed
   int* block_table = nullptr;
+  int* bt_shadow = nullptr;  // delayed write-through: block table with the window on scratch pages
   SvState* st = nullptr;
   bf16 *x = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
   float* x_ss = nullptr;
@@ -184,6 +186,25 @@ cudaError_t run_linear(sv_ctx* ctx, const LinearDesc& d, const LinParams& p, int
 // ------------------------------------------------------------------ the step
 enum LinWhich { LIN_QKV = 0, LIN_O = 1, LIN_GU = 2, LIN_DOWN = 3, LIN_HEAD = 4 };
 
+// Delayed write-through applies to verify steps of more than one row (a
+// single row is committed whenever the step is).
+bool step_delayed(const sv_ctx* ctx, int M, int mode) {
+  return ctx->bt_shadow != nullptr && mode == MODE_VERIFY && M > 1;
+}
+
+// The block table through which a step's kernels write and read K/V.
+const int* step_table(const sv_ctx* ctx, int M, int mode) {
+  return step_delayed(ctx, M, mode) ? ctx->bt_shadow : ctx->block_table;
+}
+
+KvDelay kv_delay(const sv_ctx* ctx, int M, int mode) {
+  KvDelay dl = {};
+  dl.bt_shadow = step_delayed(ctx, M, mode) ? ctx->bt_shadow : nullptr;
+  dl.win0 = ctx->cfg.max_pages;
+  dl.bt_len = ctx->bt_len;
+  return dl;
+}
+
 // Parameters of one linear of one step of M rows.
 LinParams lin_params(sv_ctx* ctx, int which, int l, int M, int mode, float* logits, int* epi,
                      bool* norm, const LinearDesc** desc) {
@@ -196,7 +217,7 @@ LinParams lin_params(sv_ctx* ctx, int which, int l, int M, int mode, float* logi
   p.ffn = c.ffn;
   p.head_dim = d;
   p.ws = ctx->ws;
-  p.block_table = ctx->block_table;
+  p.block_table = step_table(ctx, M, mode);
   p.rope = ctx->rope;
   p.n_q_heads = Hq;
   p.n_kv_heads = c.n_kv_heads;
@@ -264,11 +285,11 @@ LinParams lin_params(sv_ctx* ctx, int which, int l, int M, int mode, float* logi
   return p;
 }
 
-AttnParams attn_params(sv_ctx* ctx, int l, int M) {
+AttnParams attn_params(sv_ctx* ctx, int l, int M, int mode) {
   const sv_config& c = ctx->cfg;
   AttnParams ap = {};
   ap.q = ctx->q;
-  ap.block_table = ctx->block_table;
+  ap.block_table = step_table(ctx, M, mode);
   ap.st = ctx->st;
   ap.part_ml = ctx->part_ml;
   ap.part_o = ctx->part_o;
@@ -277,7 +298,7 @@ AttnParams attn_params(sv_ctx* ctx, int l, int M) {
   ap.n_q_heads = c.n_q_heads;
   ap.n_kv_heads = c.n_kv_heads;
   ap.max_splits = ctx->max_splits;
-  ap.max_pages = c.max_pages;
+  ap.max_pages = ctx->pool_pages;
   ap.layer = l;
   ap.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)c.head_dim));
   return ap;
@@ -288,11 +309,16 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   const sv_config& c = ctx->cfg;
   const int H = c.hidden, d = c.head_dim, Hkv = c.n_kv_heads;
   cudaStream_t s = ctx->stream;
-  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, mode == MODE_VERIFY, s));
   // the trace hook copies the residual stream between kernels: no programmatic
   // dependent launch while it is on
   const bool tracing = ctx->trace != nullptr && M <= ctx->trace_rows;
   const bool pdl = ctx->use_pdl && !tracing;
+  const KvDelay dl = kv_delay(ctx, M, mode);
+  if (dl.bt_shadow != nullptr)
+    CK(launch_kv_window_in(ctx->kpool, ctx->vpool, ctx->layer_stride, ctx->block_table, dl, ctx->st, c.n_layers,
+                           Hkv, d, M, s));
+  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, mode == MODE_VERIFY, s,
+                  pdl && dl.bt_shadow != nullptr));
   auto trace_copy = [&](int entry) -> cudaError_t {
     if (!tracing) return cudaSuccess;
     return cudaMemcpyAsync(ctx->trace + (size_t)entry * M * H, ctx->x, (size_t)M * H * sizeof(bf16),
@@ -327,7 +353,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
     LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
     if (l == 0) p.withhold_cta1 = ctx->withhold_cta1;
     CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_QKV, l)));
-    AttnParams ap = attn_params(ctx, l, M);
+    AttnParams ap = attn_params(ctx, l, M, mode);
     CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, pdl));
     CK(launch_attn_combine(ap, d, s, pdl));
     for (int w : {LIN_O, LIN_GU, LIN_DOWN}) {
@@ -341,7 +367,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
     CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_HEAD, 0)));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
-                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, s, pdl));
+                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, dl, s, pdl));
   return SV_OK;
 }
 
@@ -394,6 +420,9 @@ int ensure_pages(sv_ctx* ctx, int len) {
   ctx->n_alloc = need;
   CK(cudaMemcpyAsync(ctx->block_table + first, ctx->pin_bt + first, (need - first) * sizeof(int),
                      cudaMemcpyHostToDevice, ctx->stream));
+  if (ctx->bt_shadow)
+    CK(cudaMemcpyAsync(ctx->bt_shadow + first, ctx->pin_bt + first, (need - first) * sizeof(int),
+                       cudaMemcpyHostToDevice, ctx->stream));
   return SV_OK;
 }
 
@@ -475,6 +504,7 @@ int validate(const sv_config* c) {
   if (c->act != 0 && c->act != 1) return 0;
   if (c->page_size != kPage || c->max_k < 1 || c->max_k > kMaxK) return 0;
   if (c->max_seq < c->max_k || c->max_seq > kMaxSeq || c->max_pages < 1) return 0;
+  if (c->kv_delayed != 0 && c->kv_delayed != 1) return 0;
   return 1;
 }
 
@@ -557,7 +587,11 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   // ---- device memory
   const int MP = mp_of(kMaxK);  // prefill blocks take kMaxK rows whatever max_k is
   ctx->bt_len = pages_for(c.max_seq);
-  ctx->layer_stride = (size_t)c.max_pages * Hkv * kPage * d;
+  ctx->pool_pages = c.max_pages + (c.kv_delayed ? kWinPages : 0);
+  ctx->layer_stride = (size_t)ctx->pool_pages * Hkv * kPage * d;
+  // kernels address the pools' rows of head_dim elements with 32-bit indices
+  if ((size_t)ctx->pool_pages * Hkv * kPage * (L > 0 ? L : 1) >= (size_t)INT32_MAX)
+    return bail(SV_E_INVAL);
   const size_t pool = ctx->layer_stride * (L > 0 ? L : 1);
   ctx->max_splits = attn_n_splits(c.max_seq, d);
   size_t ws_words = 0;
@@ -585,6 +619,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->am_val, (size_t)kMaxK * ctx->lin_head.n_tiles)) ||
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
+  if (c.kv_delayed && (rc = dalloc(ctx, &ctx->bt_shadow, (size_t)ctx->bt_len))) return bail(rc);
   if (cudaMemset(ctx->ws_tc, 0xff, ws_words * sizeof(uint32_t)) != cudaSuccess) return bail(SV_E_CUDA);
   if (!make_bf16_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
       !make_bf16_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
@@ -599,7 +634,9 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
     return bail(SV_E_NOMEM);
   for (int i = 0; i < ctx->bt_len; ++i) ctx->pin_bt[i] = -1;
   if (cudaMemcpy(ctx->block_table, ctx->pin_bt, sizeof(int) * ctx->bt_len, cudaMemcpyHostToDevice) !=
-      cudaSuccess)
+          cudaSuccess ||
+      (ctx->bt_shadow &&
+       cudaMemcpy(ctx->bt_shadow, ctx->pin_bt, sizeof(int) * ctx->bt_len, cudaMemcpyHostToDevice) != cudaSuccess))
     return bail(SV_E_CUDA);
   for (int pg = c.max_pages - 1; pg >= 0; --pg) ctx->free_pages.push_back(pg);
   if (launch_rope_table(ctx->rope, c.max_seq, d, c.rope_theta, ctx->stream) != cudaSuccess ||
@@ -845,7 +882,7 @@ int sv_spec_generate(sv_ctx* target, sv_ctx* draft, int32_t pending, int K, int 
 
 int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head) {
   if (!ctx || K < 1) return SV_E_INVAL;
-  return 1 + 6 * ctx->cfg.n_layers + (with_head ? 2 : 1);
+  return 1 + 6 * ctx->cfg.n_layers + (with_head ? 2 : 1) + (with_head && step_delayed(ctx, K, MODE_VERIFY) ? 1 : 0);
 }
 
 int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, double* bytes_per_launch) {

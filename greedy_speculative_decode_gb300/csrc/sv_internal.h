@@ -104,6 +104,19 @@ struct SvState {
   int32_t state_err;    // a step was rejected since the host last looked (cleared by sv_sync)
 };
 
+// Delayed K/V write-through (sv_config.kv_delayed): during a verify step the
+// window's logical pages pos/16 .. pos/16 + kWinPages - 1 are mapped, in a
+// shadow block table, to kWinPages scratch pages at the end of each layer's
+// pool, which first receive a copy of the real pages; the step writes and
+// reads the window there, and only the rows it accepts are copied into the
+// real pages afterwards.  A window of up to 32 rows spans at most 3 pages.
+constexpr int kWinPages = 3;
+struct KvDelay {
+  int* bt_shadow;  // null: write-then-truncate
+  int win0;        // first scratch page of each layer
+  int bt_len;      // entries of the block tables
+};
+
 struct LinParams {
   // the weight in the tiled layout (see LinearDesc::tiled), or null: the
   // producer then reads the row-major weight through the kernel's tensor map
@@ -192,13 +205,21 @@ size_t linear_smem_bytes(int mt);
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
                              int head_dim, int grid, bool multi, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_combine(const AttnParams& p, int head_dim, cudaStream_t s, bool pdl);
-// check: a verify step, whose tokens[0] must equal st->pending when that is known
+// check: a verify step, whose tokens[0] must equal st->pending when that is known.
+// pdl: launched as a programmatic dependent of the delayed write-through
+// window copy (the kernel then ends only after the copy has).
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
-                         SvState* st, bool check, cudaStream_t s);
+                         SvState* st, bool check, cudaStream_t s, bool pdl);
 cudaError_t launch_accept(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                           int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                           const int* block_table, int n_layers, int n_kv_heads, int head_dim,
-                          cudaStream_t s, bool pdl);
+                          const KvDelay& dl, cudaStream_t s, bool pdl);
+// Delayed write-through, before a verify step of M rows: map the window's
+// pages to the scratch pages in the shadow table and copy the real pages'
+// contents there (zeros for pages not yet held).
+cudaError_t launch_kv_window_in(bf16* kpool, bf16* vpool, size_t layer_stride, const int* block_table,
+                                const KvDelay& dl, const SvState* st, int n_layers, int n_kv_heads,
+                                int head_dim, int M, cudaStream_t s);
 cudaError_t launch_rope_table(float2* tab, int max_seq, int head_dim, float theta, cudaStream_t s);
 cudaError_t launch_kv_zero(bf16* kpool, bf16* vpool, size_t layer_stride, const int* block_table,
                            int n_layers, int n_kv_heads, int head_dim, int first, int last,

@@ -79,6 +79,20 @@ typedef struct {
   float rms_eps, rope_theta;
   int32_t qk_norm, act, tie_embeddings;
   int32_t page_size, max_pages, max_k, max_seq;
+  /* kv_delayed: when to write a verify window's K/V into the cache.
+   *   0 = write-then-truncate: the step writes every window row into the
+   *       cache pages and, after acceptance, zeroes the rejected rows.
+   *   1 = delayed write-through ("Phase B decision — post-v4", section
+   *       "Phase C gating item (new)", candidate C0 "Delayed KV write-through":
+   *       verify produces its logits without committing K/V; K/V are committed
+   *       once acceptance is decided): the window is written into three
+   *       scratch pages per layer (seeded with the committed rows of its pages)
+   *       and only the accepted rows are copied into the cache.  Rejected
+   *       drafts never reach the cache pages.
+   *   Both give bit-identical logits, argmax, acceptance and cache contents;
+   *   1 costs 3 more pages per layer and one copy kernel per verify step.
+   *   Prefill and decode steps commit every row and take path 0 either way. */
+  int32_t kv_delayed;
 } sv_config;
 
 /* Device pointers to bf16 weights, row-major, borrowed for the context's
@@ -240,8 +254,9 @@ int sv_shuffle_pages(sv_ctx* ctx, uint64_t seed);
  * The buffer must stay valid while it is set. */
 int sv_trace_hidden(sv_ctx* ctx, void* hidden_dev, int max_rows);
 
-/* Number of kernel launches in one step of K rows, with (1) or without (0)
- * the LM head and acceptance. */
+/* Number of kernel launches in one step of K rows: with_head = 1 counts a
+ * verify step (LM head and acceptance, and for kv_delayed with K > 1 the
+ * window copy), 0 a prefill block without the LM head. */
 int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head);
 
 /* Measurement hook for the dominant kernel class.  Launches one linear of the

@@ -18,9 +18,9 @@ def make(cfg, seed=0, gain_std=0.1, host=True):
     return hw, dw
 
 
-def context(cfg, dw, max_k=8, max_seq=512, max_pages=None, shuffle=None):
+def context(cfg, dw, max_k=8, max_seq=512, max_pages=None, shuffle=None, kv_delayed=False):
     import greedy_speculative_decode_gb300 as sv
-    ctx = sv.Context(cfg, dw, max_k=max_k, max_seq=max_seq, max_pages=max_pages)
+    ctx = sv.Context(cfg, dw, max_k=max_k, max_seq=max_seq, max_pages=max_pages, kv_delayed=kv_delayed)
     if shuffle is not None:
         ctx.shuffle_pages(shuffle)
     return ctx
