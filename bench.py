@@ -458,10 +458,12 @@ def run_prefill(args):
         dt = time.perf_counter() - t0
         if r > 0:
             best = dt if best is None else min(best, dt)
-    blocks = math.ceil(n / sv.MAX_K)
+    sizes = sv.prefill_blocks(n, use_tc=os.environ.get("SV_NO_TC") != "1")
+    blocks = len(sizes)
     streamed = blocks * cfg.weight_bytes() + n * cfg.kv_bytes_per_token()
     print(json.dumps({"mode": "prefill", "config": cfg.name, "tokens": n, "max_k": args.K,
-                      "row_block": sv.MAX_K, "seconds": best, "tok_s": n / best,
+                      "row_blocks": sizes if len(sizes) <= 12 else sizes[:6] + ["..."] + sizes[-2:],
+                      "seconds": best, "tok_s": n / best,
                       "weight_passes": blocks, "streamed_GB": streamed / 1e9,
                       "hbm_frac": streamed / best / 1e9 / hbm_peak}))
 

@@ -16,6 +16,7 @@ SV_OK, SV_E_INVAL, SV_E_NOMEM, SV_E_CUDA, SV_E_STATE = 0, -1, -2, -3, -4
 SV_LIN_O, SV_LIN_GATE_UP, SV_LIN_DOWN, SV_LIN_LM_HEAD = 1, 2, 3, 4
 PAGE_SIZE = 16
 MAX_K = 32
+MAX_PREFILL_ROWS = 128
 _ERRNAMES = {SV_E_INVAL: "SV_E_INVAL", SV_E_NOMEM: "SV_E_NOMEM", SV_E_CUDA: "SV_E_CUDA",
              SV_E_STATE: "SV_E_STATE"}
 
@@ -64,6 +65,7 @@ def _load():
     L.sv_shuffle_pages.argtypes = [_P, ctypes.c_uint64]
     L.sv_trace_hidden.argtypes = [_P, _P, _i32]
     L.sv_step_kernel_count.argtypes = [_P, _i32, _i32]
+    L.sv_prefill_blocks.argtypes = [_i32, _i32, _P, _i32]
     L.sv_spec_generate.argtypes = [_P, _P, _i32, _i32, _i32, _P, _P, _P, _P]
     L.sv_time_linear.argtypes = [_P, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_float),
                                  ctypes.POINTER(ctypes.c_double)]
@@ -73,7 +75,7 @@ def _load():
     for name in ("sv_create", "sv_prefill", "sv_decode", "sv_verify", "sv_verify_async",
                  "sv_reserve", "sv_sync", "sv_truncate", "sv_seq_len", "sv_kv_read",
                  "sv_shuffle_pages", "sv_trace_hidden", "sv_step_kernel_count", "sv_time_linear",
-                 "sv_lm_head_noalloc"):
+                 "sv_lm_head_noalloc", "sv_prefill_blocks"):
         getattr(L, name).restype = _i32
     return L
 
@@ -148,6 +150,18 @@ def spec_generate(target: "Context", draft: "Context", pending: int, K: int, n_n
                                         ctypes.byref(n_out), ctypes.byref(nxt), stats))
     return (list(out[:n_out.value]), nxt.value,
             {"verify_steps": stats[0], "accepted": stats[1], "proposed": stats[2]})
+
+
+def prefill_blocks(n: int, use_tc: bool = True) -> list:
+    """sv_prefill_blocks: the row blocks sv_prefill cuts n prompt tokens into
+    (use_tc: the context runs the tcgen05 linears, the default)."""
+    cnt = _lib.sv_prefill_blocks(int(n), 1 if use_tc else 0, None, 0)
+    if cnt < 0:
+        raise SvError(cnt, f"no prefill of {n} tokens")
+    arr = (ctypes.c_int32 * cnt)()
+    if _lib.sv_prefill_blocks(int(n), 1 if use_tc else 0, ctypes.cast(arr, _P), cnt) != cnt:
+        raise SvError(SV_E_INVAL, "prefill schedule changed size")
+    return list(arr)
 
 
 class Context:

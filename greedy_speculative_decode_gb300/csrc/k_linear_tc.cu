@@ -1,15 +1,17 @@
-// k_linear_tc.cu -- the batch-invariant linear for blocks of 9 to 32 rows on
+// k_linear_tc.cu -- the batch-invariant linear for blocks of 9 to 128 rows on
 // the fifth-generation tensor cores (tcgen05): Y[m, n] = sum_k X[m, k] W[n, k].
 //
 // Same weight stream, split and epilogues as the mma.sync form, with the
 // multiply moved off the consumer warps.  Each ring stage holds a 128-row x
-// 64-column weight block (two TMA boxes) and the 32 x 64 block of the input
-// rows at the same columns (one TMA box; rows past M are never stored).  One
-// thread issues, per block, four tcgen05.mma of 128 x N x 16 (weight rows as
-// the 128-row operand, the token rows padded to N = 16 or 32 as the N-column
-// one) into an fp32 accumulator in tensor memory; a tile piece (a CTA's run
-// of k-blocks inside one 128-row tile) starts from zero, and two accumulators
-// alternate so the next piece runs while the consumers read the last one back.
+// 64-column weight block and the 32 x 64 (or, for prefill blocks of more
+// than 32 rows, 128 x 64) block of the input rows at the same columns (one
+// TMA box; rows past M are never stored).  One thread issues, per block, four
+// tcgen05.mma of 128 x N x 16 (weight rows as the 128-row operand, the token
+// rows padded to N = 16, 32 or 128 as the N-column one) into an fp32
+// accumulator in tensor memory; a tile piece (a CTA's run of k-blocks inside
+// one 128-row tile) starts from zero, and two accumulators alternate so the
+// next piece runs while the consumers read the last one back, 32 token rows
+// at a time.
 //
 // Bit-identity with the mma.sync form (and so with single-token decode):
 // every output element is the fp32 sum of the same products taken 16 k at a
@@ -28,14 +30,20 @@
 namespace sv {
 namespace {
 
-constexpr int kTcStages = 8;
-constexpr int kTcMP = 32;                                  // most padded token rows (the 32-row form)
-constexpr int kTcXBytes = kTcMP * 128;                     // 32 rows x 64 columns, 128B-swizzled
-constexpr int kTcStageBytes = kLinStageBytes + kTcXBytes;  // 20 KB, a multiple of 1024
 constexpr int kTcThreads = (kLinConsumerWarps + 2) * 32;
 constexpr int kTcProducerWarp = kLinConsumerWarps, kTcMmaWarp = kLinConsumerWarps + 1;
-constexpr int kTcCols = 2 * kTcMP;                         // tensor-memory columns: two accumulators of up to 32
-static_assert(kTcStageBytes % 1024 == 0, "swizzle atoms stay aligned");
+
+// Geometry of the form for MP padded token rows (16, 32 or 128).
+template <int MP>
+struct TcGeom {
+  static constexpr int kXRows = MP <= 32 ? 32 : MP;                   // rows of the input box
+  static constexpr int kStageBytes = kLinStageBytes + kXRows * 128;  // weight block + input box
+  static constexpr int kStages = MP <= 32 ? 8 : 6;
+  static constexpr int kAcc = MP <= 32 ? 32 : MP;    // tensor-memory columns between the two accumulators
+  static constexpr int kCols = MP <= 32 ? 64 : 256;  // tensor-memory columns allocated (a power of 2)
+  static constexpr int kCR = MP <= 32 ? MP : 32;     // token rows per read-back / epilogue chunk
+  static_assert(kStageBytes % 1024 == 0, "swizzle atoms stay aligned");
+};
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory operand descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -90,8 +98,8 @@ __device__ __forceinline__ void tc_ld8(uint32_t taddr, float* v) {
 
 // ---------------------------------------------------------------- layout
 struct TcSmem {
-  uint8_t* ring;        // [kTcStages][W 16 KB | X 4 KB]
-  float* T;             // [128][kTcMP + 1] epilogue tile
+  uint8_t* ring;        // [S][weight 16 KB | input box]
+  float* T;             // [128][kCR + 1] epilogue tile
   uint64_t* full;       // [S] the stage's weight and input bytes landed
   uint64_t* xnorm;      // [S] the stage's input rows are normalised (by one consumer warp)
   uint64_t* empty;      // [S] the multiplies reading the stage completed
@@ -100,37 +108,50 @@ struct TcSmem {
   uint64_t* drain;      // the issuer's last multiplies completed
   uint64_t* gbar;       // the gain window landed
   bf16* gs;             // [kLinXCols] gain of the CTA's input window (norm prologue)
-  float* s_rstd;        // [kMaxK]
+  float* s_rstd;        // [MP]
   float* s_hrstd;       // [64]
   uint32_t* taddr;      // tensor-memory base address from tcgen05.alloc
 };
 
+template <int MP>
 __device__ __forceinline__ TcSmem tc_smem(uint8_t* smem) {
+  using G = TcGeom<MP>;
   TcSmem sm;
   sm.ring = smem;
-  sm.T = reinterpret_cast<float*>(smem + kTcStages * kTcStageBytes);
+  sm.T = reinterpret_cast<float*>(smem + G::kStages * G::kStageBytes);
   sm.full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm.T) +
-                                        ((kLinRows * (kTcMP + 1) * sizeof(float) + 15) & ~size_t(15)));
-  sm.xnorm = sm.full + kTcStages;
-  sm.empty = sm.xnorm + kTcStages;
-  sm.acc_full = sm.empty + kTcStages;
+                                        ((kLinRows * (G::kCR + 1) * sizeof(float) + 15) & ~size_t(15)));
+  sm.xnorm = sm.full + G::kStages;
+  sm.empty = sm.xnorm + G::kStages;
+  sm.acc_full = sm.empty + G::kStages;
   sm.acc_empty = sm.acc_full + 2;
   sm.drain = sm.acc_empty + 2;
   sm.gbar = sm.drain + 1;
   sm.gs = reinterpret_cast<bf16*>(sm.gbar + 1);
   sm.s_rstd = reinterpret_cast<float*>(sm.gs + kLinXCols);
-  sm.s_hrstd = sm.s_rstd + kMaxK;
+  sm.s_hrstd = sm.s_rstd + MP;
   sm.taddr = reinterpret_cast<uint32_t*>(sm.s_hrstd + 64);
   return sm;
 }
+
+template <int MP>
+constexpr size_t tc_smem_bytes() {
+  using G = TcGeom<MP>;
+  return 1024 /* alignment slack */ + (size_t)G::kStages * G::kStageBytes +
+         (((size_t)kLinRows * (G::kCR + 1) * sizeof(float) + 15) & ~size_t(15)) +
+         (3 * G::kStages + 6) * sizeof(uint64_t) + kLinXCols * sizeof(bf16) + (MP + 64) * sizeof(float) + 16;
+}
+static_assert(tc_smem_bytes<128>() <= 232448, "fits the per-block shared-memory limit");
 
 // ---------------------------------------------------------------- producer
 // One thread.  The weight boxes of the first S blocks go out before the wait
 // on the previous kernel (weights never depend on it), their input boxes
 // after it; then both for each block as its stage frees up.  Returns the
 // number of blocks issued through `issued` and false on a timeout.
+template <int MP>
 __device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CUtensorMap* xmap, int cta,
                            int G, const TcSmem& sm, long long& issued) {
+  constexpr int S = TcGeom<MP>::kStages, SB = TcGeom<MP>::kStageBytes;
   const int KB = p.Kd / kLinBK;
   long long kb_begin, kb_end;
   lin_range(p, cta, G, kb_begin, kb_end);
@@ -140,10 +161,10 @@ __device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CU
   if (n <= 0) return true;
   int tile = (int)(kb_begin / KB), kk = (int)(kb_begin % KB);
   auto weight = [&](int s) {
-    load_weight_block(p, wmap, sm.ring + s * kTcStageBytes, tile, kk, &sm.full[s], pol_w);
+    load_weight_block(p, wmap, sm.ring + s * SB, tile, kk, &sm.full[s], pol_w);
   };
   auto input = [&](int s, int kcol) {
-    tma_load_2d(sm.ring + s * kTcStageBytes + kLinStageBytes, xmap, kcol * kLinBK, 0, &sm.full[s], pol_x);
+    tma_load_2d(sm.ring + s * SB + kLinStageBytes, xmap, kcol * kLinBK, 0, &sm.full[s], pol_x);
   };
   auto advance = [&]() {
     if (++kk == KB) {
@@ -151,10 +172,10 @@ __device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CU
       ++tile;
     }
   };
-  const int pre = (int)(n < kTcStages ? n : kTcStages);
+  const int pre = (int)(n < S ? n : S);
   const int kk_first = kk;
   for (int s = 0; s < pre; ++s) {
-    mbar_arrive_expect_tx(&sm.full[s], kTcStageBytes);
+    mbar_arrive_expect_tx(&sm.full[s], SB);
     weight(s);
     advance();
   }
@@ -165,9 +186,9 @@ __device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CU
   }
   issued = pre;
   for (long long i = pre; i < n; ++i) {
-    const int s = (int)(i % kTcStages);
-    if (!mbar_wait(&sm.empty[s], (uint32_t)((i / kTcStages) & 1) ^ 1u)) return false;
-    mbar_arrive_expect_tx(&sm.full[s], kTcStageBytes);
+    const int s = (int)(i % S);
+    if (!mbar_wait(&sm.empty[s], (uint32_t)((i / S) & 1) ^ 1u)) return false;
+    mbar_arrive_expect_tx(&sm.full[s], SB);
     weight(s);
     input(s, kk);
     advance();
@@ -177,9 +198,10 @@ __device__ bool tc_produce(const LinParams& p, const CUtensorMap* wmap, const CU
 }
 
 // Wait (bounded) until the copies of the last use of every stage landed.
+template <int MP>
 __device__ void tc_produce_drain(const TcSmem& sm, long long issued) {
-  for (long long u = issued - 1; u >= 0 && u >= issued - kTcStages; --u)
-    mbar_wait(&sm.full[u % kTcStages], (uint32_t)((u / kTcStages) & 1));
+  constexpr int S = TcGeom<MP>::kStages;
+  for (long long u = issued - 1; u >= 0 && u >= issued - S; --u) mbar_wait(&sm.full[u % S], (uint32_t)((u / S) & 1));
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -192,6 +214,7 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
   long long kb_begin, kb_end;
   lin_range(p, cta, G, kb_begin, kb_end);
   constexpr uint32_t idesc = tc_idesc(kLinRows, MP);
+  constexpr int S = TcGeom<MP>::kStages, SB = TcGeom<MP>::kStageBytes;
   long long left = kb_end - kb_begin;
   int kk0 = (int)(kb_begin % KB);
   long long it = 0;
@@ -205,10 +228,10 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
       break;
     }
     tc_fence_after();
-    const uint32_t d_tmem = tmem + (uint32_t)(b * kTcMP);  // buffers 32 columns apart
+    const uint32_t d_tmem = tmem + (uint32_t)(b * TcGeom<MP>::kAcc);
     for (int j = 0; j < nblk; ++j, ++it) {
-      const int s = (int)(it % kTcStages);
-      const uint32_t par = (uint32_t)((it / kTcStages) & 1);
+      const int s = (int)(it % S);
+      const uint32_t par = (uint32_t)((it / S) & 1);
       if (!mbar_wait(&sm.full[s], par)) {
         ok = false;
         break;
@@ -218,7 +241,7 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
         break;
       }
       tc_fence_after();
-      const uint32_t a_base = smem_u32(sm.ring + s * kTcStageBytes), b_base = a_base + kLinStageBytes;
+      const uint32_t a_base = smem_u32(sm.ring + s * SB), b_base = a_base + kLinStageBytes;
 #pragma unroll
       for (int k16 = 0; k16 < kLinBK / 16; ++k16)
         tc_mma(d_tmem, tc_sdesc(a_base + 32 * k16), tc_sdesc(b_base + 32 * k16), idesc, j > 0 || k16 > 0);
@@ -237,7 +260,7 @@ __device__ bool tc_issue(const LinParams& p, int cta, int G, const TcSmem& sm, u
 }
 
 // ---------------------------------------------------------------- consumers
-// Split-tile exchange.  A CTA's partial slot holds 128 x 32 fp32 words,
+// Split-tile exchange.  A CTA's partial slot holds 128 x 128 fp32 words,
 // token rows in quads and tile rows innermost: the quad (c .. c + 3), c a
 // multiple of 4, of tile row lr is at words 4 (32 c + lr) .. + 3, so a warp
 // (32 consecutive tile rows) stores and polls 512 contiguous bytes per
@@ -273,7 +296,7 @@ __device__ __forceinline__ bool tc_gather(uint32_t* slots, int cta, int nseg, in
   bool ok = true;
   for (int j0 = 1; j0 < nseg; j0 += B) {
     auto addr = [&](int i) {
-      return tc_quad(slots + (size_t)(cta + j0 + i / QS) * kLinRows * kTcMP, lr, mb + 4 * (i % QS));
+      return tc_quad(slots + (size_t)(cta + j0 + i / QS) * kLinRows * kTcMaxRows, lr, mb + 4 * (i % QS));
     };
     uint4 x[NQ];
     uint32_t live = 0;
@@ -348,7 +371,9 @@ __device__ __forceinline__ void tc_row_rstd(const LinParams& p, const TcSmem& sm
 
 template <int EPI, bool NORM, int MP>
 __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, const TcSmem& sm, uint32_t tmem) {
-  constexpr int TS = MP + 1, CW = MP / 2;  // CW: token rows per consumer warp
+  using Geo = TcGeom<MP>;
+  constexpr int S = Geo::kStages, SB = Geo::kStageBytes;
+  constexpr int CR = Geo::kCR, TS = CR + 1, CW = CR / 2;  // chunk rows; CW: a warp's token rows of a chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nthr = kLinConsumerWarps * 32;
   const int KB = p.Kd / kLinBK;
@@ -379,11 +404,13 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
     if (gain_staged && !mbar_wait(sm.gbar, 0)) ok = false;
     named_sync(1, nthr);
   }
-  // accumulator read-back: warp w owns tensor-memory lanes (tile rows)
-  // 32 (w mod 4) + lane and token rows mb .. mb + CW - 1
+  // accumulator read-back, CR token rows (one chunk) at a time: warp w owns
+  // tensor-memory lanes (tile rows) 32 (w mod 4) + lane and the chunk's token
+  // rows mb .. mb + CW - 1
   const int lr = 32 * (warp & 3) + lane, mb = CW * (warp >> 2);
+  const int nch = (p.M + CR - 1) / CR;  // chunks that hold rows
   float* T = sm.T;
-  EpiPre<MP> pre;
+  EpiPre<CR> pre;
   long long it = 0;
   int piece = 0;
   int tile = (int)(kb_begin / KB), kk0 = (int)(kb_begin % KB);
@@ -391,27 +418,26 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
   while (left > 0) {
     const int nblk = (int)(left < KB - kk0 ? left : KB - kk0);
     if (NORM) {
-      // block `it` is normalised by consumer warp it mod 8, so eight blocks
-      // are in hand at once; lane l takes the 16-byte chunk l mod 8 of rows
+      // block `it` is normalised by consumer warp it mod S, so S blocks are
+      // in hand at once and every use of a stage has the same owner (waits
+      // on a stage's barrier then never run two phases ahead, where the
+      // parity would alias); lane l takes the 16-byte chunk l mod 8 of rows
       // 4 i + l / 8 (four rows of 128 contiguous bytes per access: no bank
       // conflicts).  128B swizzle: chunk pc of row m holds columns
       // 8 (pc ^ (m mod 8)) .. + 7 of the block.
+      static_assert(S <= kLinConsumerWarps, "a consumer warp per stage");
       for (int j = 0; j < nblk; ++j, ++it) {
-        // Every use of stage s then has the same owner, warp s: a warp never
-        // waits on a stage's barrier two phases ahead, where the parity
-        // test would alias and pass early.  That needs one warp per stage.
-        static_assert(kTcStages == kLinConsumerWarps, "one owner warp per ring stage");
-        if ((int)(it % kLinConsumerWarps) != warp) continue;
-        const int s = (int)(it % kTcStages);
-        if (ok && !mbar_wait(&sm.full[s], (uint32_t)((it / kTcStages) & 1))) ok = false;
+        if ((int)(it % S) != warp) continue;
+        const int s = (int)(it % S);
+        if (ok && !mbar_wait(&sm.full[s], (uint32_t)((it / S) & 1))) ok = false;
         if (ok) {
-          uint8_t* xb = sm.ring + s * kTcStageBytes + kLinStageBytes;
+          uint8_t* xb = sm.ring + s * SB + kLinStageBytes;
           const int pc = lane & 7;
           int wc = (kk0 + j) * kLinBK - c0;  // window column of the block
           if (wc < 0) wc += p.Kd;
           const uint4* g = gain_staged ? reinterpret_cast<const uint4*>(sm.gs + wc)
                                        : reinterpret_cast<const uint4*>(p.gain + (kk0 + j) * kLinBK);
-#pragma unroll
+#pragma unroll 4
           for (int i = 0; i < MP / 4; ++i) {
             const int m = 4 * i + (lane >> 3);
             if (m < p.M) {
@@ -431,53 +457,66 @@ __device__ bool tc_consume(const LinParams& p, uint32_t* slots, int cta, int G, 
     left -= nblk;
     ++tile;
     kk0 = 0;
-    float v[CW];
     const int b = piece & 1;
     if (ok && !mbar_wait(&sm.acc_full[b], (uint32_t)((piece / 2) & 1))) ok = false;
     tc_fence_after();
-    if (ok) {
-      const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(b * kTcMP + mb);
-#pragma unroll
-      for (int c = 0; c < CW; c += 8) tc_ld8(ta + c, v + c);
-    } else {
-#pragma unroll
-      for (int c = 0; c < CW; ++c) v[c] = 0.0f;
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
     ++piece;
-    if (kk_first != 0) {
-      // A later segment of a split tile (the first piece of this CTA's
-      // range): leave the partial in this CTA's slot (its words were empty)
-      // and move on.
-      uint32_t* slot = slots + (size_t)cta * kLinRows * kTcMP;
+    const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(b * Geo::kAcc + mb);
+    for (int ch = 0; ch < nch; ++ch) {
+      const int r0 = ch * CR;  // first token row of the chunk
+      float v[CW];
+      if (ok) {
 #pragma unroll
-      for (int c = 0; c < CW; c += 4)
-        if (mb + c < p.M)
-          st_relaxed_v4_u32(tc_quad(slot, lr, mb + c), __float_as_uint(v[c]), __float_as_uint(v[c + 1]),
-                            __float_as_uint(v[c + 2]), __float_as_uint(v[c + 3]));
-      continue;
-    }
-    epi_preload<MP, EPI>(p, tile_done, pos, cap, pre);
-    if (kk != KB - 1) {
-      // The first segment of a split tile (the last piece of this CTA's
-      // range): add the later segments' partials in k order.
-      const int nseg = owner_cta((long long)tile_done * KB + KB - 1, Tk, G) - cta + 1;
-      if (!tc_gather<CW>(slots, cta, nseg, lr, mb, p.M, v)) ok = false;
-    }
-    named_sync(1, nthr);  // the previous tile's epilogue is done with T
+        for (int c = 0; c < CW; c += 8) tc_ld8(ta + r0 + c, v + c);
+      } else {
 #pragma unroll
-    for (int c = 0; c < CW; ++c) T[lr * TS + mb + c] = v[c];
-    named_sync(1, nthr);
-    if (EPI == EPI_QKV)
-      epilogue_qkv<MP>(p, tile_done, T, TS, sm.s_hrstd, pos, pre);
-    else if (EPI == EPI_RESID)
-      epilogue_resid<MP>(p, tile_done, T, TS, pre);
-    else if (EPI == EPI_GLU)
-      epilogue_glu(p, tile_done, T, TS);
-    else
-      epilogue_logits<MP>(p, tile_done, T, TS);
+        for (int c = 0; c < CW; ++c) v[c] = 0.0f;
+      }
+      if (ch == nch - 1) {  // the accumulator is free once its last chunk is in registers
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+      }
+      if (kk_first != 0) {
+        // A later segment of a split tile (the first piece of this CTA's
+        // range): leave the partial in this CTA's slot and move on.
+        uint32_t* slot = slots + (size_t)cta * kLinRows * kTcMaxRows;
+#pragma unroll
+        for (int c = 0; c < CW; c += 4)
+          if (r0 + mb + c < p.M)
+            st_relaxed_v4_u32(tc_quad(slot, lr, r0 + mb + c), __float_as_uint(v[c]), __float_as_uint(v[c + 1]),
+                              __float_as_uint(v[c + 2]), __float_as_uint(v[c + 3]));
+        continue;
+      }
+      // The chunk's rows r0 .. r0 + CR - 1 as an epilogue of up to CR rows:
+      // the same epilogue code, its row pointers and positions moved by r0.
+      LinParams pc = p;
+      if (MP > CR) {
+        pc.M = min(CR, p.M - r0);
+        pc.out = p.out + (size_t)r0 * p.out_stride;
+        if (EPI == EPI_RESID) pc.out_ss = p.out_ss + (size_t)r0 * p.n_tiles;
+      }
+      const int pos_c = pos + r0;
+      epi_preload<CR, EPI>(pc, tile_done, pos_c, cap, pre);
+      if (kk != KB - 1) {
+        // The first segment of a split tile (the last piece of this CTA's
+        // range): add the later segments' partials in k order.
+        const int nseg = owner_cta((long long)tile_done * KB + KB - 1, Tk, G) - cta + 1;
+        if (!tc_gather<CW>(slots, cta, nseg, lr, r0 + mb, p.M, v)) ok = false;
+      }
+      named_sync(1, nthr);  // the previous epilogue is done with T
+#pragma unroll
+      for (int c = 0; c < CW; ++c) T[lr * TS + mb + c] = v[c];
+      named_sync(1, nthr);
+      if (EPI == EPI_QKV)
+        epilogue_qkv<CR>(pc, tile_done, T, TS, sm.s_hrstd, pos_c, pre);
+      else if (EPI == EPI_RESID)
+        epilogue_resid<CR>(pc, tile_done, T, TS, pre);
+      else if (EPI == EPI_GLU)
+        epilogue_glu(pc, tile_done, T, TS);
+      else
+        epilogue_logits<CR>(pc, tile_done, T, TS);
+    }
   }
   return ok;
 }
@@ -491,10 +530,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  const TcSmem sm = tc_smem(smem);
+  using Geo = TcGeom<MP>;
+  const TcSmem sm = tc_smem<MP>(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
+    for (int s = 0; s < Geo::kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.xnorm[s], 1);
       mbar_init(&sm.empty[s], 1);
@@ -509,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp == 0) {  // one warp allocates (and later frees) the two accumulators
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(sm.taddr)),
-                 "n"(kTcCols)
+                 "n"(Geo::kCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -524,9 +564,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&xmap);
       long long issued = 0;
-      ok = tc_produce(p, &wmap, &xmap, blockIdx.x, gridDim.x, sm, issued);
+      ok = tc_produce<MP>(p, &wmap, &xmap, blockIdx.x, gridDim.x, sm, issued);
       if (ok) lin_prefetch_next(p, &pfmap, blockIdx.x);
-      tc_produce_drain(sm, issued);
+      tc_produce_drain<MP>(sm, issued);
     }
   } else if (warp == kTcMmaWarp) {
     if (lane == 0) ok = tc_issue<NORM, MP>(p, blockIdx.x, gridDim.x, sm, tmem);
@@ -538,7 +578,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(Geo::kCols)
+                 : "memory");
   }
 }
 
@@ -548,7 +589,7 @@ cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.grid);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = linear_tc_smem_bytes();
+  cfg.dynamicSmemBytes = tc_smem_bytes<MP>();
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -558,13 +599,21 @@ cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* 
   return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM, MP>, d.map, pfmap, xmap, p, slots);
 }
 
+template <int EPI, bool NORM, int MP>
+cudaError_t prepare_tc_mp() {
+  return cudaFuncSetAttribute(k_linear_tc<EPI, NORM, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc_smem_bytes<MP>());
+}
+
 template <int EPI, bool NORM>
 cudaError_t prepare_tc_t() {
-  cudaError_t e = cudaFuncSetAttribute(k_linear_tc<EPI, NORM, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)linear_tc_smem_bytes());
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_linear_tc<EPI, NORM, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)linear_tc_smem_bytes());
+  cudaError_t e;
+  if ((e = prepare_tc_mp<EPI, NORM, 16>()) != cudaSuccess) return e;
+  if ((e = prepare_tc_mp<EPI, NORM, 32>()) != cudaSuccess) return e;
+  if constexpr (EPI == EPI_LOGITS)
+    return cudaSuccess;  // the LM head runs on at most 32 rows
+  else
+    return prepare_tc_mp<EPI, NORM, 128>();
 }
 
 template <int MP>
@@ -577,20 +626,18 @@ cudaError_t launch_tc_mp(const LinearDesc& d, const CUtensorMap& xmap, uint32_t*
       return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false, MP>(d, xmap, slots, p, s, pdl, pf);
     case EPI_GLU:
       return norm ? launch_tc_t<EPI_GLU, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
-    case EPI_LOGITS:
-      return norm ? launch_tc_t<EPI_LOGITS, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_LOGITS:  // the LM head runs on at most 32 rows
+      if (MP > 32) return cudaErrorInvalidValue;
+      return norm ? launch_tc_t<EPI_LOGITS, true, (MP > 32 ? 32 : MP)>(d, xmap, slots, p, s, pdl, pf)
+                  : cudaErrorInvalidValue;
   }
   return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-size_t linear_tc_smem_bytes() {
-  size_t b = 1024;  // alignment slack
-  b += (size_t)kTcStages * kTcStageBytes;
-  b += ((size_t)kLinRows * (kTcMP + 1) * sizeof(float) + 15) & ~size_t(15);
-  b += (3 * kTcStages + 6) * sizeof(uint64_t) + kLinXCols * sizeof(bf16) + (kMaxK + 64) * sizeof(float) + 16;
-  return b;
+size_t linear_tc_smem_bytes(int mp) {
+  return mp <= 16 ? tc_smem_bytes<16>() : (mp <= 32 ? tc_smem_bytes<32>() : tc_smem_bytes<128>());
 }
 
 cudaError_t prepare_linear_tc_kernels() {
@@ -603,7 +650,7 @@ cudaError_t prepare_linear_tc_kernels() {
 
 cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p_in,
                              int epi, bool norm, cudaStream_t s, bool pdl, const LinearDesc* next) {
-  if (p_in.M < 1 || p_in.M > kTcMP) return cudaErrorInvalidValue;
+  if (p_in.M < 1 || p_in.M > kTcMaxRows) return cudaErrorInvalidValue;
   LinParams p = p_in;
   if (next) {
     p.pf_blocks = kLinPrefetchBlocks;
@@ -612,12 +659,15 @@ cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, uint3
     p.pf_grid = next->grid;
     p.pf_map = next->map_kind;
     p.pf_ffn = next->N / 2;  // gate|up: the up rows start at ffn
+    p.pf_wt = next->tiled;
   } else {
     p.pf_blocks = 0;
+    p.pf_wt = nullptr;
   }
   const CUtensorMap& pf = next ? next->map : d.map;
   if (p.M <= 16) return launch_tc_mp<16>(d, xmap, slots, p, epi, norm, s, pdl, pf);
-  return launch_tc_mp<32>(d, xmap, slots, p, epi, norm, s, pdl, pf);
+  if (p.M <= 32) return launch_tc_mp<32>(d, xmap, slots, p, epi, norm, s, pdl, pf);
+  return launch_tc_mp<128>(d, xmap, slots, p, epi, norm, s, pdl, pf);
 }
 
 }  // namespace sv

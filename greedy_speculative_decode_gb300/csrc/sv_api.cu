@@ -39,7 +39,8 @@ struct sv_ctx {
   std::vector<LinearDesc> lin_qkv, lin_o, lin_gu, lin_down;
   LinearDesc lin_head;
   CUtensorMap kmap, vmap;
-  CUtensorMap xmap_x, xmap_o, xmap_a;  // input rows of the linears, [kMaxK rows] x 64-column boxes
+  // input rows of the tcgen05 linears: boxes of 64 columns x 32 rows, and x 128 rows
+  CUtensorMap xmap_x, xmap_o, xmap_a, xmap128_x, xmap128_o, xmap128_a;
   // device memory owned by the context
   std::vector<void*> allocs;
   bf16 *kpool = nullptr, *vpool = nullptr;
@@ -173,11 +174,23 @@ int dalloc(sv_ctx* ctx, T** p, size_t count) {
 
 int mp_of(int M) { return M <= 8 ? 8 : (M <= 16 ? 16 : 32); }
 
+// Rows of the next prefill block when `rest` prompt tokens are left: the
+// last block takes the 1..kMaxK rows left over, the others kMaxK rows, or
+// with the tcgen05 linear up to kTcMaxRows (a multiple of kMaxK).
+int prefill_block(int rest, bool use_tc) {
+  const int tail = (rest - 1) % kMaxK + 1;
+  if (rest == tail) return rest;
+  return use_tc ? std::min(kTcMaxRows, rest - tail) : kMaxK;
+}
+
 // One linear of a step: blocks of more than 8 rows go to the tcgen05 form.
 cudaError_t run_linear(sv_ctx* ctx, const LinearDesc& d, const LinParams& p, int epi, bool norm,
                        cudaStream_t s, bool pdl, const LinearDesc* next) {
   if (ctx->use_tc && p.M > 8) {
-    const CUtensorMap* xm = p.X == ctx->x ? &ctx->xmap_x : (p.X == ctx->o ? &ctx->xmap_o : &ctx->xmap_a);
+    const bool big = p.M > kMaxK;
+    const CUtensorMap* xm = p.X == ctx->x ? (big ? &ctx->xmap128_x : &ctx->xmap_x)
+                                          : (p.X == ctx->o ? (big ? &ctx->xmap128_o : &ctx->xmap_o)
+                                                           : (big ? &ctx->xmap128_a : &ctx->xmap_a));
     return launch_linear_tc(d, *xm, ctx->ws_tc, p, epi, norm, s, pdl, next);
   }
   return launch_linear(d, p, epi, norm, s, pdl, next);
@@ -317,8 +330,11 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   if (dl.bt_shadow != nullptr)
     CK(launch_kv_window_in(ctx->kpool, ctx->vpool, ctx->layer_stride, ctx->block_table, dl, ctx->st, c.n_layers,
                            Hkv, d, M, s));
-  CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, mode == MODE_VERIFY, s,
-                  pdl && dl.bt_shadow != nullptr));
+  // (blocks of more than kMaxK rows are embedded before the step, kMaxK rows
+  // at a time: see sv_prefill)
+  if (M <= kMaxK)
+    CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, mode == MODE_VERIFY, s,
+                    pdl && dl.bt_shadow != nullptr));
   auto trace_copy = [&](int entry) -> cudaError_t {
     if (!tracing) return cudaSuccess;
     return cudaMemcpyAsync(ctx->trace + (size_t)entry * M * H, ctx->x, (size_t)M * H * sizeof(bf16),
@@ -605,26 +621,33 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
     acc_ws(ctx->lin_down[l]);
   }
   acc_ws(ctx->lin_head);
+  // the tcgen05 form's slots hold kTcMaxRows token rows; activations hold a
+  // prefill block of kTcMaxRows rows (a step takes at most kMaxK)
+  const size_t ws_tc_words = ws_words / MP * kTcMaxRows;
+  const int kRows = std::max(kMaxK, kTcMaxRows);
   if ((rc = dalloc(ctx, &ctx->kpool, pool)) || (rc = dalloc(ctx, &ctx->vpool, pool)) ||
       (rc = dalloc(ctx, &ctx->block_table, (size_t)ctx->bt_len)) || (rc = dalloc(ctx, &ctx->st, 1)) ||
-      (rc = dalloc(ctx, &ctx->x, (size_t)kMaxK * H)) ||
-      (rc = dalloc(ctx, &ctx->q, (size_t)kMaxK * Hq * d)) ||
-      (rc = dalloc(ctx, &ctx->o, (size_t)kMaxK * Hq * d)) ||
-      (rc = dalloc(ctx, &ctx->a, (size_t)kMaxK * c.ffn)) ||
-      (rc = dalloc(ctx, &ctx->x_ss, (size_t)kMaxK * (H / 128))) ||
+      (rc = dalloc(ctx, &ctx->x, (size_t)kRows * H)) ||
+      (rc = dalloc(ctx, &ctx->q, (size_t)kRows * Hq * d)) ||
+      (rc = dalloc(ctx, &ctx->o, (size_t)kRows * Hq * d)) ||
+      (rc = dalloc(ctx, &ctx->a, (size_t)kRows * c.ffn)) ||
+      (rc = dalloc(ctx, &ctx->x_ss, (size_t)kRows * (H / 128))) ||
       (rc = dalloc(ctx, &ctx->rope, (size_t)c.max_seq * (d / 2))) ||
-      (rc = dalloc(ctx, &ctx->part_ml, (size_t)kMaxK * Hq * ctx->max_splits)) ||
-      (rc = dalloc(ctx, &ctx->part_o, (size_t)kMaxK * Hq * ctx->max_splits * d)) ||
-      (rc = dalloc(ctx, &ctx->ws, ws_words)) || (rc = dalloc(ctx, &ctx->ws_tc, ws_words)) ||
+      (rc = dalloc(ctx, &ctx->part_ml, (size_t)kRows * Hq * ctx->max_splits)) ||
+      (rc = dalloc(ctx, &ctx->part_o, (size_t)kRows * Hq * ctx->max_splits * d)) ||
+      (rc = dalloc(ctx, &ctx->ws, ws_words)) || (rc = dalloc(ctx, &ctx->ws_tc, ws_tc_words)) ||
       (rc = dalloc(ctx, &ctx->am_val, (size_t)kMaxK * ctx->lin_head.n_tiles)) ||
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
   if (c.kv_delayed && (rc = dalloc(ctx, &ctx->bt_shadow, (size_t)ctx->bt_len))) return bail(rc);
-  if (cudaMemset(ctx->ws_tc, 0xff, ws_words * sizeof(uint32_t)) != cudaSuccess) return bail(SV_E_CUDA);
+  if (cudaMemset(ctx->ws_tc, 0xff, ws_tc_words * sizeof(uint32_t)) != cudaSuccess) return bail(SV_E_CUDA);
   if (!make_bf16_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
       !make_bf16_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
-      !make_bf16_map(&ctx->xmap_x, ctx->x, kMaxK, H, kMaxK) || !make_bf16_map(&ctx->xmap_o, ctx->o, kMaxK, Hq * d, kMaxK) ||
-      !make_bf16_map(&ctx->xmap_a, ctx->a, kMaxK, c.ffn, kMaxK))
+      !make_bf16_map(&ctx->xmap_x, ctx->x, kRows, H, kMaxK) || !make_bf16_map(&ctx->xmap_o, ctx->o, kRows, Hq * d, kMaxK) ||
+      !make_bf16_map(&ctx->xmap_a, ctx->a, kRows, c.ffn, kMaxK) ||
+      !make_bf16_map(&ctx->xmap128_x, ctx->x, kRows, H, kTcMaxRows) ||
+      !make_bf16_map(&ctx->xmap128_o, ctx->o, kRows, Hq * d, kTcMaxRows) ||
+      !make_bf16_map(&ctx->xmap128_a, ctx->a, kRows, c.ffn, kTcMaxRows))
     return bail(SV_E_CUDA);
   // a prefill of max_seq tokens stages every block [cap_len, tokens] side by side
   ctx->pin_in_len = (size_t)c.max_seq + (c.max_seq + kMaxK - 1) / kMaxK + kMaxK + 8;
@@ -687,6 +710,20 @@ int sv_decode(sv_ctx* ctx, int32_t token, float* logits_dev, int32_t* next_token
   return sv_verify(ctx, &token, 1, logits_dev, &n, next_token);
 }
 
+int sv_prefill_blocks(int n, int use_tc, int32_t* sizes, int max_blocks) {
+  if (n < 1) return SV_E_INVAL;
+  int count = 0;
+  for (int done = 0; done < n; ++count) {
+    const int M = prefill_block(n - done, use_tc != 0);
+    if (sizes) {
+      if (count >= max_blocks) return SV_E_INVAL;
+      sizes[count] = M;
+    }
+    done += M;
+  }
+  return count;
+}
+
 int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logits_dev,
                int32_t* next_token) {
   if (!ctx) return SV_E_INVAL;
@@ -697,17 +734,32 @@ int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logit
     return fail(ctx, SV_E_INVAL, "length %d + %d exceeds max_seq", ctx->seq_len, n);
   if ((rc = begin_call(ctx))) return rc;
   if ((rc = ensure_pages(ctx, ctx->seq_len + n))) return rc;
-  // blocks of as many rows as a step holds, whatever max_k: each block streams
-  // every weight once, and no row's arithmetic depends on the block's size
-  const int B = kMaxK;
+  // Each block streams every weight once, and no row's arithmetic depends on
+  // the block's size, so the blocks are as large as the kernels allow: the
+  // last one (whose final row gives the next token) has the 1..kMaxK rows
+  // left over, the others kMaxK rows each, or up to kTcMaxRows with the
+  // tcgen05 linear.  Blocks of more than kMaxK rows are embedded here, kMaxK
+  // rows at a time, before their step.
+  const int H = ctx->cfg.hidden;
   int at = 0;
-  for (int done = 0; done < n; done += B) {
-    const int M = std::min(B, n - done);
+  for (int done = 0; done < n;) {
+    const int M = prefill_block(n - done, ctx->use_tc);
     const bool last = done + M == n;
-    if ((rc = upload_tokens(ctx, tokens_host + done, M, at))) return rc;
-    at += M + 1;
+    if (M > kMaxK) {
+      for (int r = 0; r < M; r += kMaxK) {
+        const int mr = std::min(kMaxK, M - r);
+        if ((rc = upload_tokens(ctx, tokens_host + done + r, mr, at))) return rc;
+        at += mr + 1;
+        CK(launch_embed(ctx->embed, H, ctx->cfg.vocab, mr, ctx->x + (size_t)r * H,
+                        ctx->x_ss + (size_t)r * (H / 128), ctx->st, false, ctx->stream, false));
+      }
+    } else {
+      if ((rc = upload_tokens(ctx, tokens_host + done, M, at))) return rc;
+      at += M + 1;
+    }
     if ((rc = run_step(ctx, M, last ? MODE_PREFILL : MODE_BODY, last ? last_logits_dev : nullptr)))
       return rc;
+    done += M;
   }
   int32_t res[4];
   if ((rc = finish_sync_step(ctx, res))) return rc;

@@ -62,7 +62,8 @@ extern "C" {
                                  pending, or tokens[0] not the pending greedy token) */
 
 #define SV_PAGE_SIZE 16       /* positions per KV page */
-#define SV_MAX_K 32           /* most rows in one verify / prefill block */
+#define SV_MAX_K 32           /* most rows in one verify step */
+#define SV_MAX_PREFILL_ROWS 128 /* most rows in one prefill block (tcgen05 linears) */
 
 typedef struct sv_ctx sv_ctx;
 
@@ -145,14 +146,15 @@ typedef struct {
 int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_ctx** out);
 void sv_destroy(sv_ctx* ctx);
 
-/* Commit n tokens (host array) at positions len .. len+n-1, processed in
- * row blocks of up to 32 rows (whatever max_k is).  last_logits_dev: device
- * fp32 [vocab] for the logits after the last token, or NULL.  next_token: the
- * greedy token after the last one (the new pending token).  Any ids may be
- * committed.  The K/V of every position are bit-identical to those of
- * one-token commits ("Shape and cache history in Gemma block verification",
- * section "Same-prefix controls": one fresh prefill of the committed prefix is
- * one of the three cache histories that must agree).  Synchronous. */
+/* Commit n tokens (host array) at positions len .. len+n-1, processed in the
+ * row blocks sv_prefill_blocks gives (whatever max_k is; each block streams
+ * every weight once).  last_logits_dev: device fp32 [vocab] for the logits
+ * after the last token, or NULL.  next_token: the greedy token after the
+ * last one (the new pending token).  Any ids may be committed.  The K/V of
+ * every position are bit-identical to those of one-token commits, whatever
+ * the block sizes ("Shape and cache history in Gemma block verification",
+ * section "Same-prefix controls": one fresh prefill of the committed prefix
+ * is one of the three cache histories that must agree).  Synchronous. */
 int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logits_dev,
                int32_t* next_token);
 
@@ -258,6 +260,16 @@ int sv_trace_hidden(sv_ctx* ctx, void* hidden_dev, int max_rows);
  * verify step (LM head and acceptance, and for kv_delayed with K > 1 the
  * window copy), 0 a prefill block without the LM head. */
 int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head);
+
+/* The row blocks sv_prefill cuts n tokens into, in order, written to
+ * sizes[0 .. count-1]; returns count, or SV_E_INVAL if n < 1 or more than
+ * max_blocks blocks would be needed (sizes may be NULL to ask for the count
+ * only, with max_blocks 0).  The last block holds the 1..SV_MAX_K rows left
+ * over; the others hold SV_MAX_K rows, or with use_tc (the tcgen05 linears,
+ * the default unless SV_NO_TC=1 was set when the context was created) up to
+ * SV_MAX_PREFILL_ROWS rows, always a multiple of SV_MAX_K.  Host only: needs
+ * no context and no GPU. */
+int sv_prefill_blocks(int n, int use_tc, int32_t* sizes, int max_blocks);
 
 /* Measurement hook for the dominant kernel class.  Launches one linear of the
  * model for K rows, once per layer (distinct weights, so every launch streams

@@ -1,6 +1,7 @@
-"""The tcgen05 form of the linear (blocks of 9 to 32 rows) against the
-mma.sync form: the same prefill and verify steps on two contexts, one with the
-tcgen05 form switched off (SV_NO_TC=1), give byte-identical logits, K/V,
+"""The tcgen05 form of the linear (blocks of 9 to 32 rows, and prefill blocks
+of up to 128) against the mma.sync form: the same prefill and verify steps on
+two contexts, one with the tcgen05 form switched off (SV_NO_TC=1, which also
+cuts prefills into 32-row blocks), give byte-identical logits, K/V,
 acceptance and corrections.  Run on the full-width 0.6B-, 8B- and Gemma-like
 shapes cut to two layers, so every weight shape, head layout, K partition and
 split-tile exchange of the full models goes through both forms."""
@@ -84,3 +85,49 @@ def test_rows_of_a_wide_block_equal_decode(model, monkeypatch, K):
     for r in range(K):
         assert torch.equal(lgK[r].view(torch.int32), rows[r][0].view(torch.int32)), f"row {r}"
     _same_cache(cfg, dec, ver)
+
+
+@pytest.mark.parametrize("n", [87, 300, 1024])
+def test_prefill_in_wide_blocks_equals_one_token_commits(model, n):
+    """A prompt committed by sv_prefill, whose blocks of up to 128 rows run
+    the tcgen05 linears with a 128-column accumulator (the 8B and Gemma-like
+    shapes stream more k-blocks per CTA than the ring has stages, so every
+    stage is reused), leaves the same K/V and next token as one-token
+    commits."""
+    cfg, dw = model
+    import greedy_speculative_decode_gb300 as sv
+    assert max(sv.prefill_blocks(n)) > sv.MAX_K
+    prompt = inputs.prefix_tokens(500 + n, n, cfg.vocab)
+    ref = gh.context(cfg, dw, max_k=4, max_seq=n + 8)
+    t = None
+    for tok in prompt:  # one-row commits of forced ids (a one-token prefill is a one-row step)
+        t = ref.prefill([tok])
+    big = gh.context(cfg, dw, max_k=4, max_seq=n + 8, shuffle=7)
+    assert big.prefill(prompt) == t
+    _same_cache(cfg, ref, big)
+
+
+def test_wide_prefill_repeats_exactly(model):
+    """Sixteen prefills of one 300-token prompt (blocks of 128, 128, 32 and 12
+    rows) into one context, truncated to zero in between so that the graphs
+    replay and the pages are reused, each equal to the first byte for byte:
+    a race in the 128-row form (ring stage reuse, the accumulator hand-off,
+    the chunked read-back, the split-tile exchange) would show up as a rare
+    difference here."""
+    cfg, dw = model
+    prompt = inputs.prefix_tokens(77, 300, cfg.vocab)
+    ctx = gh.context(cfg, dw, max_k=4, max_seq=320, shuffle=3)
+    first = None
+    for rep in range(16):
+        ctx.truncate(0)
+        lg = gh.logits_buf(1, cfg.vocab)
+        t = ctx.prefill(prompt, logits=lg)
+        kv = [tuple(x.view(torch.int16).clone() for x in ctx.kv_read(layer, 0, 300)) for layer in range(cfg.n_layers)]
+        if first is None:
+            first = (t, lg.clone(), kv)
+            continue
+        assert t == first[0], f"repeat {rep}: next token"
+        assert torch.equal(lg.view(torch.int32), first[1].view(torch.int32)), f"repeat {rep}: logits"
+        for layer in range(cfg.n_layers):
+            assert torch.equal(kv[layer][0], first[2][layer][0]), f"repeat {rep}: K of layer {layer}"
+            assert torch.equal(kv[layer][1], first[2][layer][1]), f"repeat {rep}: V of layer {layer}"

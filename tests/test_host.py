@@ -119,3 +119,33 @@ def test_schedule_follows_acceptance_rule():
     assert inputs.window(chain, 0, 8, vocab=1000)[1] == 7
     assert inputs.window(chain, 0, 8, vocab=1000, reject_at=0)[1] == 0
     assert inputs.window(chain, 0, 8, vocab=1000, reject_at=4)[1] == 4
+
+
+@pytest.mark.parametrize("n", [1, 2, 31, 32, 33, 64, 65, 87, 100, 128, 129, 160, 161, 300, 1024, 4096, 4097])
+def test_prefill_block_schedule(n):
+    """sv_prefill_blocks (host only): the blocks cover the prompt in order;
+    the last holds the 1..32 rows left over; the others hold 32 rows, or up
+    to 128 rows (a multiple of 32) with the tcgen05 linears, as large as
+    allowed, so a 1024-token prompt streams the weights 9 times, not 32."""
+    import greedy_speculative_decode_gb300 as sv
+    for use_tc in (False, True):
+        sizes = sv.prefill_blocks(n, use_tc=use_tc)
+        assert sum(sizes) == n and all(s >= 1 for s in sizes)
+        assert sizes[-1] == (n - 1) % sv.MAX_K + 1
+        cap = sv.MAX_PREFILL_ROWS if use_tc else sv.MAX_K
+        for s in sizes[:-1]:
+            assert s % sv.MAX_K == 0 and s <= cap
+        # greedy: every block but the last two is full
+        assert all(s == cap for s in sizes[:-2])
+    assert len(sv.prefill_blocks(1024, use_tc=True)) == 9
+    assert len(sv.prefill_blocks(1024, use_tc=False)) == 32
+
+
+def test_prefill_block_schedule_rejects_bad_calls():
+    import ctypes
+
+    import greedy_speculative_decode_gb300 as sv
+    L = sv.lib()
+    assert L.sv_prefill_blocks(0, 1, None, 0) == sv.SV_E_INVAL
+    arr = (ctypes.c_int32 * 2)()
+    assert L.sv_prefill_blocks(300, 1, ctypes.cast(arr, ctypes.c_void_p), 2) == sv.SV_E_INVAL
