@@ -599,6 +599,35 @@ cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* 
   return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM, MP>, d.map, pfmap, xmap, p, slots);
 }
 
+// RMS-normalised input rows for the 128-row form: xn[m, :] =
+// bf16(bf16(x[m, :] rstd_m) gain), rstd_m from the per-128-column sums of
+// squares in tc_row_rstd's order (lane-strided sums, then an xor tree), so
+// xn holds exactly the values the norm prologue would write into every ring
+// stage, once instead of once per weight tile.  Block (c, m): row m, 16-byte
+// vectors c * 256 + threadIdx.x, ...
+__global__ void __launch_bounds__(256) k_norm_rows(const bf16* __restrict__ x, const float* __restrict__ x_ss,
+                                                   const bf16* __restrict__ gain, bf16* __restrict__ xn, int H,
+                                                   int ss_tiles, float eps) {
+  pdl_trigger();
+  pdl_wait();  // x and its sums of squares come from the previous kernel
+  const int m = blockIdx.y;
+  __shared__ float s_r;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float ss = 0.0f;
+    for (int t = lane; t < ss_tiles; t += 32) ss = __fadd_rn(ss, __ldcg(x_ss + m * ss_tiles + t));
+    for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    if (lane == 0) s_r = 1.0f / sqrtf(ss / (float)H + eps);
+  }
+  __syncthreads();
+  const float r = s_r;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)m * H);
+  uint4* yr = reinterpret_cast<uint4*>(xn + (size_t)m * H);
+  for (int c8 = blockIdx.x * blockDim.x + threadIdx.x; c8 < H / 8; c8 += gridDim.x * blockDim.x)
+    yr[c8] = norm8(__ldcg(xr + c8), r, __ldg(reinterpret_cast<const uint4*>(gain) + c8));
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // read next through TMA
+}
+
 template <int EPI, bool NORM, int MP>
 cudaError_t prepare_tc_mp() {
   return cudaFuncSetAttribute(k_linear_tc<EPI, NORM, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -610,10 +639,13 @@ cudaError_t prepare_tc_t() {
   cudaError_t e;
   if ((e = prepare_tc_mp<EPI, NORM, 16>()) != cudaSuccess) return e;
   if ((e = prepare_tc_mp<EPI, NORM, 32>()) != cudaSuccess) return e;
-  if constexpr (EPI == EPI_LOGITS)
+  if constexpr (EPI == EPI_LOGITS) {
     return cudaSuccess;  // the LM head runs on at most 32 rows
-  else
+  } else {
+    if constexpr (NORM)  // 128-row blocks take their rows normalised by k_norm_rows
+      if ((e = prepare_tc_mp<EPI, false, 128>()) != cudaSuccess) return e;
     return prepare_tc_mp<EPI, NORM, 128>();
+  }
 }
 
 template <int MP>
@@ -621,10 +653,14 @@ cudaError_t launch_tc_mp(const LinearDesc& d, const CUtensorMap& xmap, uint32_t*
                          int epi, bool norm, cudaStream_t s, bool pdl, const CUtensorMap& pf) {
   switch (epi) {
     case EPI_QKV:
+      if constexpr (MP == 128)  // the 128-row form also takes pre-normalised rows
+        if (!norm) return launch_tc_t<EPI_QKV, false, MP>(d, xmap, slots, p, s, pdl, pf);
       return norm ? launch_tc_t<EPI_QKV, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
     case EPI_RESID:
       return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false, MP>(d, xmap, slots, p, s, pdl, pf);
     case EPI_GLU:
+      if constexpr (MP == 128)
+        if (!norm) return launch_tc_t<EPI_GLU, false, MP>(d, xmap, slots, p, s, pdl, pf);
       return norm ? launch_tc_t<EPI_GLU, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
     case EPI_LOGITS:  // the LM head runs on at most 32 rows
       if (MP > 32) return cudaErrorInvalidValue;
@@ -635,6 +671,20 @@ cudaError_t launch_tc_mp(const LinearDesc& d, const CUtensorMap& xmap, uint32_t*
 }
 
 }  // namespace
+
+cudaError_t launch_norm_rows(const bf16* x, const float* x_ss, const bf16* gain, bf16* xn, int M, int H,
+                             float eps, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((H / 8 + 255) / 256, M);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_norm_rows, x, x_ss, gain, xn, H, H / 128, eps);
+}
 
 size_t linear_tc_smem_bytes(int mp) {
   return mp <= 16 ? tc_smem_bytes<16>() : (mp <= 32 ? tc_smem_bytes<32>() : tc_smem_bytes<128>());

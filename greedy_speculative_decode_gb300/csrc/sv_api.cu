@@ -40,7 +40,7 @@ struct sv_ctx {
   LinearDesc lin_head;
   CUtensorMap kmap, vmap;
   // input rows of the tcgen05 linears: boxes of 64 columns x 32 rows, and x 128 rows
-  CUtensorMap xmap_x, xmap_o, xmap_a, xmap128_x, xmap128_o, xmap128_a;
+  CUtensorMap xmap_x, xmap_o, xmap_a, xmap128_x, xmap128_o, xmap128_a, xmap128_xn;
   // device memory owned by the context
   std::vector<void*> allocs;
   bf16 *kpool = nullptr, *vpool = nullptr;
@@ -50,6 +50,7 @@ struct sv_ctx {
   int* bt_shadow = nullptr;  // delayed write-through: block table with the window on scratch pages
   SvState* st = nullptr;
   bf16 *x = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
+  bf16* xn = nullptr;  // normalised input rows of a prefill block of more than kMaxK rows
   float* x_ss = nullptr;
   float2* rope = nullptr;
   float2* part_ml = nullptr;
@@ -188,9 +189,10 @@ cudaError_t run_linear(sv_ctx* ctx, const LinearDesc& d, const LinParams& p, int
                        cudaStream_t s, bool pdl, const LinearDesc* next) {
   if (ctx->use_tc && p.M > 8) {
     const bool big = p.M > kMaxK;
-    const CUtensorMap* xm = p.X == ctx->x ? (big ? &ctx->xmap128_x : &ctx->xmap_x)
-                                          : (p.X == ctx->o ? (big ? &ctx->xmap128_o : &ctx->xmap_o)
-                                                           : (big ? &ctx->xmap128_a : &ctx->xmap_a));
+    const CUtensorMap* xm = p.X == ctx->xn ? &ctx->xmap128_xn
+                            : p.X == ctx->x ? (big ? &ctx->xmap128_x : &ctx->xmap_x)
+                                            : (p.X == ctx->o ? (big ? &ctx->xmap128_o : &ctx->xmap_o)
+                                                             : (big ? &ctx->xmap128_a : &ctx->xmap_a));
     return launch_linear_tc(d, *xm, ctx->ws_tc, p, epi, norm, s, pdl, next);
   }
   return launch_linear(d, p, epi, norm, s, pdl, next);
@@ -365,15 +367,27 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
       default: return c.n_layers > 0 ? &ctx->lin_qkv[0] : nullptr;
     }
   };
+  // Blocks of more than kMaxK rows (prefill) normalise the input rows of QKV
+  // and gate|up once, in a kernel of their own, instead of in every CTA's
+  // ring stage for every weight tile: the same values (k_norm_rows).
+  auto prenorm = [&](LinParams& p, bool& nm) -> cudaError_t {
+    if (M <= kMaxK || !nm || !ctx->use_tc) return cudaSuccess;
+    cudaError_t e = launch_norm_rows(p.X, p.x_ss, p.gain, ctx->xn, M, H, c.rms_eps, s, pdl);
+    p.X = ctx->xn;
+    nm = false;
+    return e;
+  };
   for (int l = 0; l < c.n_layers; ++l) {
     LinParams p = lin_params(ctx, LIN_QKV, l, M, mode, logits, &epi, &norm, &ld);
     if (l == 0) p.withhold_cta1 = ctx->withhold_cta1;
+    CK(prenorm(p, norm));
     CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_QKV, l)));
     AttnParams ap = attn_params(ctx, l, M, mode);
     CK(launch_attention(ctx->kmap, ctx->vmap, ap, d, attn_grid, attn_multi, s, pdl));
     CK(launch_attn_combine(ap, d, s, pdl));
     for (int w : {LIN_O, LIN_GU, LIN_DOWN}) {
       p = lin_params(ctx, w, l, M, mode, logits, &epi, &norm, &ld);
+      CK(prenorm(p, norm));
       CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(w, l)));
     }
     CK(trace_copy(l + 1));
@@ -627,7 +641,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   const int kRows = std::max(kMaxK, kTcMaxRows);
   if ((rc = dalloc(ctx, &ctx->kpool, pool)) || (rc = dalloc(ctx, &ctx->vpool, pool)) ||
       (rc = dalloc(ctx, &ctx->block_table, (size_t)ctx->bt_len)) || (rc = dalloc(ctx, &ctx->st, 1)) ||
-      (rc = dalloc(ctx, &ctx->x, (size_t)kRows * H)) ||
+      (rc = dalloc(ctx, &ctx->x, (size_t)kRows * H)) || (rc = dalloc(ctx, &ctx->xn, (size_t)kRows * H)) ||
       (rc = dalloc(ctx, &ctx->q, (size_t)kRows * Hq * d)) ||
       (rc = dalloc(ctx, &ctx->o, (size_t)kRows * Hq * d)) ||
       (rc = dalloc(ctx, &ctx->a, (size_t)kRows * c.ffn)) ||
@@ -646,6 +660,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       !make_bf16_map(&ctx->xmap_x, ctx->x, kRows, H, kMaxK) || !make_bf16_map(&ctx->xmap_o, ctx->o, kRows, Hq * d, kMaxK) ||
       !make_bf16_map(&ctx->xmap_a, ctx->a, kRows, c.ffn, kMaxK) ||
       !make_bf16_map(&ctx->xmap128_x, ctx->x, kRows, H, kTcMaxRows) ||
+      !make_bf16_map(&ctx->xmap128_xn, ctx->xn, kRows, H, kTcMaxRows) ||
       !make_bf16_map(&ctx->xmap128_o, ctx->o, kRows, Hq * d, kTcMaxRows) ||
       !make_bf16_map(&ctx->xmap128_a, ctx->a, kRows, c.ffn, kTcMaxRows))
     return bail(SV_E_CUDA);
