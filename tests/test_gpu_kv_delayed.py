@@ -83,10 +83,11 @@ def test_delayed_matches_write_then_truncate_tiny(K, prompt_len, shuffle):
 
 def test_delayed_matches_8b_shaped_layers():
     """8B-shaped layers (8 kv heads of 128), 2 layers, shuffled pages of a
-    32-page pool (ids 0..31; the scratch pages are ids 32..34)."""
+    32-page pool (ids 0..31; the scratch pages are ids 32..34), after a
+    300-token prompt prefilled in 128-row blocks."""
     cfg = inputs.shrink(inputs.QWEN3_8B, n_layers=2, vocab=32768)
     _, dw = gh.make(cfg, seed=3, gain_std=0.1, host=False)
-    prompt = inputs.prefix_tokens(95, 60, cfg.vocab)
+    prompt = inputs.prefix_tokens(95, 300, cfg.vocab)
     a = _sync_run(cfg, dw, prompt, 16, 5, 0.2, False, 9, max_pages=32)
     b = _sync_run(cfg, dw, prompt, 16, 5, 0.2, True, 9, max_pages=32)
     for s, (x, y) in enumerate(zip(a, b)):
@@ -142,3 +143,29 @@ def test_delayed_kernel_count():
     assert b.kernels_per_step(8) == a.kernels_per_step(8) + 1
     assert b.kernels_per_step(1) == a.kernels_per_step(1)   # a decode step commits its row directly
     assert b.kernels_per_step(8, with_head=False) == a.kernels_per_step(8, with_head=False)
+
+
+def test_delayed_draft_verify_loop_matches():
+    """sv_spec_generate with an 8B-shaped target (one layer, 32768 ids) in
+    delayed mode and a 0.6B-shaped drafter of other weights, so that drafts
+    are rejected, commits the same tokens, counts and cache as with
+    write-then-truncate."""
+    import greedy_speculative_decode_gb300 as sv
+    tcfg = inputs.shrink(inputs.QWEN3_8B, n_layers=1, vocab=32768)
+    dcfg = inputs.shrink(inputs.QWEN3_0P6B, n_layers=2, vocab=32768)
+    _, tw = gh.make(tcfg, seed=0, gain_std=0.1, host=False)
+    _, dw = gh.make(dcfg, seed=1, gain_std=0.1, host=False)
+    prompt = inputs.prefix_tokens(82, 40, tcfg.vocab)
+    out = []
+    for delayed in (False, True):
+        tgt = gh.context(tcfg, tw, max_k=8, max_seq=128, kv_delayed=delayed)
+        drf = gh.context(dcfg, dw, max_k=8, max_seq=128)
+        pending = tgt.prefill(prompt)
+        drf.prefill(prompt)
+        toks, nxt, st = sv.spec_generate(tgt, drf, pending, 4, 40)
+        out.append((toks, nxt, st, _kv(tgt, tcfg, 0, _pages_end(len(tgt)))))
+        tgt.close()
+        drf.close()
+    assert out[0][:3] == out[1][:3]
+    assert out[0][2]["accepted"] < out[0][2]["proposed"], "no draft was rejected"
+    assert _same_kv(out[0][3], out[1][3])

@@ -149,3 +149,17 @@ def test_prefill_block_schedule_rejects_bad_calls():
     assert L.sv_prefill_blocks(0, 1, None, 0) == sv.SV_E_INVAL
     arr = (ctypes.c_int32 * 2)()
     assert L.sv_prefill_blocks(300, 1, ctypes.cast(arr, ctypes.c_void_p), 2) == sv.SV_E_INVAL
+
+
+@pytest.mark.parametrize("bad", [-1, 2])
+def test_create_rejects_bad_kv_delayed(bad):
+    """sv_config.kv_delayed is 0 or 1; anything else is SV_E_INVAL, decided
+    before any device work."""
+    import ctypes
+
+    import greedy_speculative_decode_gb300 as sv
+    c = sv.SvConfig(2, 256, 4, 2, 64, 704, 1024, 1e-6, 1e4, 1, 0, 1, 16, 8, 8, 128, bad)
+    w = sv.SvWeights()
+    h = ctypes.c_void_p(0)
+    assert sv.lib().sv_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == sv.SV_E_INVAL
+    assert not h.value
