@@ -81,11 +81,13 @@ def test_delayed_matches_write_then_truncate_tiny(K, prompt_len, shuffle):
         assert _same_kv(x[4], y[4]), f"step {s}: cache differs"
 
 
-def test_delayed_matches_8b_shaped_layers():
-    """8B-shaped layers (8 kv heads of 128), 2 layers, shuffled pages of a
-    32-page pool (ids 0..31; the scratch pages are ids 32..34), after a
-    300-token prompt prefilled in 128-row blocks."""
-    cfg = inputs.shrink(inputs.QWEN3_8B, n_layers=2, vocab=32768)
+@pytest.mark.parametrize("shape", ["qwen3-8b-shape", "gemma-like"])
+def test_delayed_matches_wide_layers(shape):
+    """8B-shaped (8 kv heads of 128) and Gemma-like (one kv head of 256)
+    layers, 2 layers, shuffled pages of a 32-page pool (ids 0..31; the
+    scratch pages are ids 32..34), after a 300-token prompt prefilled in
+    128-row blocks."""
+    cfg = inputs.shrink(inputs.CONFIGS[shape], n_layers=2, vocab=32768)
     _, dw = gh.make(cfg, seed=3, gain_std=0.1, host=False)
     prompt = inputs.prefix_tokens(95, 300, cfg.vocab)
     a = _sync_run(cfg, dw, prompt, 16, 5, 0.2, False, 9, max_pages=32)
