@@ -360,19 +360,37 @@ __device__ void epilogue_logits(const LinParams& p, int tile, float* T, int TS) 
   }
 }
 
+// Split-tile partial slots of this form: fp32 words [CTA][128 tile rows][MP
+// token rows].  A word not yet written holds kLinEmpty, a NaN with the sign
+// bit set: arithmetic only produces the canonical NaN 0x7fffffff, so no
+// partial sum equals it.  Each 32-bit element of a .v2 access is single-copy
+// atomic, so a word is either the value or still empty: the stores are the
+// message (no fence, no flag).  The reducer writes kLinEmpty back into every
+// word it consumed; the slots are all kLinEmpty between launches.
+constexpr uint32_t kLinEmpty = 0xffffffffu;
+
+__device__ __forceinline__ void st_relaxed_v2_u32(uint32_t* p, uint32_t a, uint32_t b) {
+  asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void ld_relaxed_v2_u32(const uint32_t* p, uint32_t& a, uint32_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "l"(p) : "memory");
+}
+
 // Reducer side of a split tile: acc holds segment 0 (this CTA's); add the
 // partials that CTAs cta + 1 ... cta + nseg - 1 left in their slots, segment
-// by segment, each thread for the elements its accumulators hold, and clear
-// the words it consumed.  The words of several segments (six for 8 padded
-// rows) are requested together and polled in rounds, so an exchange costs one
-// L2 round trip once the partials have landed.  Returns false if a partial
-// never arrived.
+// by segment, each thread for the elements its accumulators hold, and empty
+// the words it consumed.  The words of several segments (twelve for 8 padded
+// rows) are requested together and the missing ones re-requested in rounds,
+// so an exchange costs one L2 round trip once the partials have landed.
+// Returns false if a partial never arrived (bounded by kWaitLimitNs).
 template <int MT>
-__device__ __forceinline__ bool gather_partials(unsigned long long* ws, int cta, int nseg, int lr0, int q,
+__device__ __forceinline__ bool gather_partials(uint32_t* ws, int cta, int nseg, int lr0, int q,
                                                 float (&acc)[MT][4]) {
   constexpr int MP = MT * 8;
-  constexpr int B = MT == 1 ? 6 : 4 / MT;  // segments in flight (registers: 8 B MT)
-  constexpr int NP = B * MT * 2;           // word pairs per thread and batch
+  constexpr int B = MT == 1 ? 6 : (MT == 2 ? 3 : 1);  // segments in flight (registers: 4 B MT)
+  constexpr int NP = B * MT * 2;            // word pairs per thread and batch
+  static_assert(NP <= 32, "one bit per pair");
   bool ok = true;
   for (int j0 = 1; j0 < nseg; j0 += B) {
     // pair i = (segment j0 + i / (2 MT), accumulator t = (i / 2) % MT, row half i % 2)
@@ -380,24 +398,45 @@ __device__ __forceinline__ bool gather_partials(unsigned long long* ws, int cta,
       const int jj = i / (2 * MT), t = (i / 2) % MT, half = i % 2;
       return ws + (size_t)(cta + j0 + jj) * kLinRows * MP + (lr0 + 8 * half) * MP + t * 8 + 2 * q;
     };
-    unsigned long long x[NP], y[NP];
+    uint32_t x[NP], y[NP];
     uint32_t live = 0;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-      x[i] = y[i] = 0ull;
+      x[i] = y[i] = 0u;
       if (j0 + i / (2 * MT) < nseg) {
         live |= 1u << i;
-        ld_relaxed_v2_u64(addr(i), x[i], y[i]);
+        ld_relaxed_v2_u32(addr(i), x[i], y[i]);
       }
     }
-    if (!poll_pairs<NP>(addr, x, y, live)) ok = false;
+    auto missing = [&]() {
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < NP; ++i)
+        if (((live >> i) & 1u) && (x[i] == kLinEmpty || y[i] == kLinEmpty)) m |= 1u << i;
+      return m;
+    };
+    uint32_t m = missing();
+    if (m != 0) {
+      const unsigned long long t0 = globaltimer_ns();
+      for (;;) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i)
+          if ((m >> i) & 1u) ld_relaxed_v2_u32(addr(i), x[i], y[i]);
+        m = missing();
+        if (m == 0) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
+      }
+    }
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       if ((live >> i) & 1u) {
         const int t = (i / 2) % MT, half = i % 2;
-        acc[t][2 * half] = __fadd_rn(acc[t][2 * half], __uint_as_float((uint32_t)x[i]));
-        acc[t][2 * half + 1] = __fadd_rn(acc[t][2 * half + 1], __uint_as_float((uint32_t)y[i]));
-        st_relaxed_v2_u64(addr(i), 0ull, 0ull);
+        acc[t][2 * half] = __fadd_rn(acc[t][2 * half], __uint_as_float(x[i]));
+        acc[t][2 * half + 1] = __fadd_rn(acc[t][2 * half + 1], __uint_as_float(y[i]));
+        st_relaxed_v2_u32(addr(i), kLinEmpty, kLinEmpty);
       }
     }
   }
@@ -760,17 +799,17 @@ __device__ bool lin_consume(const LinParams& p, int cta, int G, const LinSmem& s
     if (kk_first != 0) {
       // A later segment of a split tile.  It is the first piece of this
       // CTA's range (every later tile starts at a tile boundary), so a CTA
-      // leaves at most one partial: in its own slot, each value one 64-bit
-      // word with tag 1 in its high half.  The stores are the message: no
-      // fence, no ticket, and nothing waits here.
-      unsigned long long* slot = p.ws + (size_t)cta * kLinRows * MP;
+      // leaves at most one partial: in its own slot (words kLinEmpty until
+      // written).  The stores are the message: no fence, no ticket, and
+      // nothing waits here.
+      uint32_t* slot = p.ws + (size_t)cta * kLinRows * MP;
       const bool withheld = cta == p.withhold_cta1 - 1;  // test hook (see LinParams)
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         const int m0 = t * 8 + 2 * q;
         if (!withheld) {
-          st_relaxed_v2_u64(slot + lr0 * MP + m0, tagged(acc[t][0]), tagged(acc[t][1]));
-          st_relaxed_v2_u64(slot + (lr0 + 8) * MP + m0, tagged(acc[t][2]), tagged(acc[t][3]));
+          st_relaxed_v2_u32(slot + lr0 * MP + m0, __float_as_uint(acc[t][0]), __float_as_uint(acc[t][1]));
+          st_relaxed_v2_u32(slot + (lr0 + 8) * MP + m0, __float_as_uint(acc[t][2]), __float_as_uint(acc[t][3]));
         }
         acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
       }

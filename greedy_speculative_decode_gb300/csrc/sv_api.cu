@@ -56,7 +56,7 @@ struct sv_ctx {
   float2* part_ml = nullptr;
   float* part_o = nullptr;
   int max_splits = 0;
-  unsigned long long* ws = nullptr;  // split-tile partial slots, one per CTA (tags start at 0)
+  uint32_t* ws = nullptr;     // split-tile partial slots, one per CTA (every byte 0xff when idle)
   uint32_t* ws_tc = nullptr;         // the same for the tcgen05 form (every byte 0xff when idle)
   float* am_val = nullptr;
   int* am_idx = nullptr;
@@ -654,7 +654,9 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       (rc = dalloc(ctx, &ctx->am_idx, (size_t)kMaxK * ctx->lin_head.n_tiles)))
     return bail(rc);
   if (c.kv_delayed && (rc = dalloc(ctx, &ctx->bt_shadow, (size_t)ctx->bt_len))) return bail(rc);
-  if (cudaMemset(ctx->ws_tc, 0xff, ws_tc_words * sizeof(uint32_t)) != cudaSuccess) return bail(SV_E_CUDA);
+  if (cudaMemset(ctx->ws, 0xff, ws_words * sizeof(uint32_t)) != cudaSuccess ||
+      cudaMemset(ctx->ws_tc, 0xff, ws_tc_words * sizeof(uint32_t)) != cudaSuccess)
+    return bail(SV_E_CUDA);
   if (!make_bf16_map(&ctx->kmap, ctx->kpool, pool / d, d, kPage) ||
       !make_bf16_map(&ctx->vmap, ctx->vpool, pool / d, d, kPage) ||
       !make_bf16_map(&ctx->xmap_x, ctx->x, kRows, H, kMaxK) || !make_bf16_map(&ctx->xmap_o, ctx->o, kRows, Hq * d, kMaxK) ||

@@ -131,10 +131,11 @@ struct LinParams {
   float eps;
   int M, Kd, n_tiles, max_seg, map, ffn, head_dim;
   int grid;      // CTAs the weight is divided over (one per SM, at most one per k-block)
-  // split-tile partials, one slot per CTA: [grid][128][MP] words {fp32 bits,
-  // tag}; a CTA whose range starts inside a tile leaves its partial of that
-  // tile in its slot (tag 1), the tile's first CTA adds it and clears it (0)
-  unsigned long long* ws;
+  // split-tile partials, one slot per CTA: [grid][128][MP] fp32 words, all
+  // 0xffffffff when idle; a CTA whose range starts inside a tile leaves its
+  // partial of that tile in its slot, the tile's first CTA adds it and puts
+  // the marker back
+  uint32_t* ws;
   // epilogue operands
   bf16* out;           // EPI_QKV: q [M, Hq d]; EPI_RESID: x [M, N] (in place); EPI_GLU: a [M, ffn]
   int out_stride;

@@ -114,7 +114,7 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   const size_t off_amv = round256(off_ss + sizeof(float) * (size_t)M * (hidden / 128));
   const size_t off_ami = round256(off_amv + sizeof(float) * (size_t)M * n_tiles);
   const size_t off_ws = round256(off_ami + sizeof(int) * (size_t)M * n_tiles);
-  const size_t ws_bytes = max_seg > 1 ? sizeof(unsigned long long) * (size_t)grid * kLinRows * mp : 0;
+  const size_t ws_bytes = max_seg > 1 ? sizeof(uint32_t) * (size_t)grid * kLinRows * mp : 0;
   const size_t end = off_ws + ws_bytes;
   if (end > kNoAllocScratchBytes) return SV_E_NOMEM;  // larger than the fixed array
 
@@ -134,7 +134,7 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   float* x_ss = reinterpret_cast<float*>(base + off_ss);
   float* am_val = reinterpret_cast<float*>(base + off_amv);
   int* am_idx = reinterpret_cast<int*>(base + off_ami);
-  unsigned long long* ws = reinterpret_cast<unsigned long long*>(base + off_ws);
+  uint32_t* ws = reinterpret_cast<uint32_t*>(base + off_ws);
 
   // Tensor map of the weight: a host-side encoding (the driver's encoder is
   // looked up once per process), no device memory.
@@ -148,10 +148,10 @@ extern "C" int sv_lm_head_noalloc(const void* x_dev, const void* gain_dev, const
   if (!make_bf16_map(&d.map, w_dev, (uint64_t)vocab, (uint64_t)hidden, 64)) return SV_E_CUDA;
 
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  // What must start at zero: the status word and the tags of the split-tile
-  // partial slots (a call that stopped early could have left them set).
+  // The status word starts at zero and every split-tile partial slot empty
+  // (0xff bytes; a call that stopped early could have left words written).
   if (cudaMemsetAsync(st, 0, sizeof(SvState), s) != cudaSuccess ||
-      (ws_bytes > 0 && cudaMemsetAsync(ws, 0, ws_bytes, s) != cudaSuccess))
+      (ws_bytes > 0 && cudaMemsetAsync(ws, 0xff, ws_bytes, s) != cudaSuccess))
     return SV_E_CUDA;
   k_rows_ss<<<dim3(hidden / 128, M), 128, 0, s>>>(static_cast<const bf16*>(x_dev), hidden, x_ss,
                                                   hidden / 128);

@@ -21,52 +21,6 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
-// ------------------------------------------- 64-bit relaxed (gpu scope) words
-// Each element of a .v2.u64 access is a single-copy-atomic 64-bit word, so a
-// word written as {value, tag} is seen either whole or not at all.
-__device__ __forceinline__ void st_relaxed_v2_u64(unsigned long long* p, unsigned long long a,
-                                                  unsigned long long b) {
-  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
-}
-
-__device__ __forceinline__ void ld_relaxed_v2_u64(const unsigned long long* p, unsigned long long& a,
-                                                  unsigned long long& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
-}
-
-// A value handed to another CTA as one word: fp32 bits low, tag 1 high.  The
-// receiver polls until the tag is set, adds the value, and stores 0 back.
-__device__ __forceinline__ unsigned long long tagged(float v) {
-  return (1ull << 32) | __float_as_uint(v);
-}
-
-// Wait (at most kWaitLimitNs) until both words of every live pair i (bit i of
-// `live`) carry their tag.  addr(i) is pair i's address, x[i], y[i] its words
-// as loaded so far.  Each round re-loads every pair still missing, all at
-// once, so a round costs one L2 round trip however many pairs are late.
-template <int N, typename Addr>
-__device__ __forceinline__ bool poll_pairs(Addr addr, unsigned long long (&x)[N], unsigned long long (&y)[N],
-                                           uint32_t live) {
-  auto missing = [&]() {
-    uint32_t m = 0;
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-      if (((live >> i) & 1u) && ((x[i] >> 32) == 0 || (y[i] >> 32) == 0)) m |= 1u << i;
-    return m;
-  };
-  uint32_t m = missing();
-  if (m == 0) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (;;) {
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-      if ((m >> i) & 1u) ld_relaxed_v2_u64(addr(i), x[i], y[i]);
-    m = missing();
-    if (m == 0) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

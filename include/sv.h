@@ -312,9 +312,9 @@ int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, doubl
  * the row statistics live in one fixed 8 MiB device array inside the library
  * (held on every GPU that loads it until the process exits).  Shapes whose
  * scratch would not fit return SV_E_NOMEM; the scratch is about
- *   8 * M * ceil(vocab/128) + 8 * G * 128 * (8, 16 or 32 for M <= 8, 16, 32)
+ *   8 * M * ceil(vocab/128) + 4 * G * 128 * (8, 16 or 32 for M <= 8, 16, 32)
  *   bytes, G <= the SM count (one CTA per SM, equal shares of W): with 152
- *   SMs a vocabulary of up to about 1.7 million ids fits at any M.
+ *   SMs a vocabulary of up to about 2.9 million ids fits at any M.
  * Other limits: 1 <= M <= 32, hidden % 128 == 0 (else SV_E_INVAL).
  * The first call on a device looks up the array's address and sets kernel
  * attributes for that device; make that first call before any stream capture.

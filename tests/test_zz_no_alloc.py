@@ -70,10 +70,12 @@ def test_no_alloc_lm_head_matches_context_full_vocab():
 
 
 def test_no_alloc_rejects_shapes_beyond_the_scratch():
-    """32 rows of a 2,000,000-id vocabulary: the argmax partials alone
-    (8 bytes per row per 128-id tile) take 4 MB, the partial slots 5 MB."""
+    """32 rows of a 3,000,000-id vocabulary: the argmax partials alone
+    (8 bytes per row per 128-id tile) take 6 MB, the split-tile slots
+    (4 bytes per tile row and padded row per CTA) 2.5 MB: more than the
+    fixed 8 MiB."""
     import greedy_speculative_decode_gb300 as sv
-    V = 2_000_000
+    V = 3_000_000
     x = torch.zeros((32, 128), dtype=torch.bfloat16, device="cuda")
     g = torch.ones((128,), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((V, 128), dtype=torch.bfloat16, device="cuda")
