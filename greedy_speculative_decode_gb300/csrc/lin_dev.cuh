@@ -30,13 +30,6 @@
 namespace sv {
 namespace {
 
-// A bf16 load that bypasses L1: the data was written by other CTAs (an
-// earlier kernel of the step, or this one), never cached here.
-__device__ __forceinline__ float ldcg_bf16(const bf16* p) {
-  unsigned short u = __ldcg(reinterpret_cast<const unsigned short*>(p));
-  return __uint_as_float((uint32_t)u << 16);
-}
-
 struct TileRows {
   int a0, b0;  // first weight row of chunk A (local rows 0..63) and chunk B (64..127)
 };
@@ -81,8 +74,11 @@ __device__ __forceinline__ float act_fn(float g, int act) {
 template <int MP>
 struct EpiPre {
   static constexpr int N = (kLinRows * MP + kLinConsumerWarps * 32 - 1) / (kLinConsumerWarps * 32);
-  float res[N];   // EPI_RESID: the residual x[m, n0 + lr]; QKV, head_dim 128: the
-                  // QK-norm gain of elements lane + 32 j (j < 4)
+  // EPI_RESID: the residual x[m, n0 + lr]; QKV, head_dim 128: the QK-norm gain
+  // of elements lane + 32 j (j < 4).  Raw bf16 bits, widened where they are
+  // used: nothing here consumes a preloaded value, so the thread goes on to
+  // request the split partials without waiting for these loads.
+  uint32_t resb[N];
   float2 cs[N];   // EPI_QKV: (cos, sin) of the element's RoPE angle
   int page[N];    // EPI_QKV: physical page of position pos + m (-1: none)
 };
@@ -99,7 +95,8 @@ __device__ __forceinline__ void epi_preload(const LinParams& p, int tile, int po
       if (m < p.M) {
         const bf16* row = p.out + (size_t)m * p.out_stride + tile * kLinRows + lane;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) pre.res[4 * k + j] = ldcg_bf16(row + 32 * j);
+        for (int j = 0; j < 4; ++j)  // written by other CTAs: bypass L1
+          pre.resb[4 * k + j] = __ldcg(reinterpret_cast<const unsigned short*>(row + 32 * j));
       }
     }
   } else if (EPI == EPI_QKV && p.head_dim == kLinRows) {
@@ -110,7 +107,7 @@ __device__ __forceinline__ void epi_preload(const LinParams& p, int tile, int po
     if (p.q_gain != nullptr && tile < p.n_q_heads + p.n_kv_heads) {  // q or k: its norm gain
       const bf16* g = kv ? p.k_gain : p.q_gain;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) pre.res[j] = __bfloat162float(g[lane + 32 * j]);
+      for (int j = 0; j < 4; ++j) pre.resb[j] = __ldg(reinterpret_cast<const unsigned short*>(g + lane + 32 * j));
     }
 #pragma unroll
     for (int k = 0; k < MP / 8; ++k) {
@@ -174,7 +171,7 @@ __device__ void epilogue_qkv(const LinParams& p, int tile, float* T, int TS, flo
         for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
         const float r = 1.0f / sqrtf(ss / (float)d + p.eps);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[j] = bf16r(__fmul_rn(bf16r(__fmul_rn(v[j], r)), pre.res[j]));
+        for (int j = 0; j < 4; ++j) v[j] = bf16r(__fmul_rn(bf16r(__fmul_rn(v[j], r)), __uint_as_float(pre.resb[j] << 16)));
       }
       float outv[4] = {v[0], v[1], v[2], v[3]};
       if (is_q || is_k) {
@@ -295,7 +292,7 @@ __device__ void epilogue_resid(const LinParams& p, int tile, float* T, int TS, c
     float ss = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const float v = bf16r(__fadd_rn(pre.res[4 * k + j], bf16r(T[(lane + 32 * j) * TS + m])));
+      const float v = bf16r(__fadd_rn(__uint_as_float(pre.resb[4 * k + j] << 16), bf16r(T[(lane + 32 * j) * TS + m])));
       row[32 * j] = __float2bfloat16_rn(v);
       ss = __fadd_rn(ss, __fmul_rn(v, v));
     }
