@@ -61,9 +61,13 @@ __global__ void __launch_bounds__(AttnCfg<D>::kThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(D) k_attn_combine(const AttnParams p) {
   pdl_trigger();
+  // The committed length is final for the whole step (only the step's last
+  // kernel, or the host between steps, changes it) and equals the step's
+  // start: read it before the wait, as the attention kernel does, so that
+  // the partials' loads are the only round trip after it.
+  const int pos = __ldcg(&p.st->seq_len);
   pdl_wait();
-  combine_element<D>(p, blockIdx.x / p.n_q_heads, blockIdx.x % p.n_q_heads, threadIdx.x,
-                     __ldcg(&p.st->step_pos));
+  combine_element<D>(p, blockIdx.x / p.n_q_heads, blockIdx.x % p.n_q_heads, threadIdx.x, pos);
 }
 
 // Longer contexts: rows of more than kCombineChunk splits take combine_long.
@@ -74,9 +78,9 @@ __global__ void __launch_bounds__(D, 768 / D) k_attn_combine_long(const AttnPara
   extern __shared__ float2 s_ml[];
   __shared__ float s_red[D / 32];
   pdl_trigger();
+  const int pos = __ldcg(&p.st->seq_len);  // final for the whole step (see k_attn_combine)
   pdl_wait();
   const int r = blockIdx.x / p.n_q_heads, hq = blockIdx.x % p.n_q_heads;
-  const int pos = __ldcg(&p.st->step_pos);
   const int ns = attn_n_splits(pos + r + 1, D);  // splits row r sees
   if (ns <= kCombineChunk)
     combine_element<D>(p, r, hq, threadIdx.x, pos);
