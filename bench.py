@@ -223,6 +223,16 @@ def ncu_traffic():
 
 
 # ------------------------------------------------------------------ CPU oracle
+def side_stream(torch):
+    """A stream of its own, made current: the library then runs on it
+    directly (on the default stream it would run on one of its own, joined
+    to the caller's at every call), and the timing events sit on the stream
+    the kernels are launched on."""
+    s = torch.cuda.Stream()
+    torch.cuda.set_stream(s)
+    return s
+
+
 def expected_tokens_per_step(K, p):
     """E[n + 1] when each draft slot matches with probability 1 - p and
     acceptance stops at the first mismatch: 1 + q + ... + q^(K-1)."""
@@ -480,7 +490,7 @@ def run_sweep(args):
     import greedy_speculative_decode_gb300 as sv
     cfg = model_config(args)
     hbm_peak, peak_kind = peaks()
-    stream = torch.cuda.current_stream()
+    stream = side_stream(torch)
     weights = inputs.device_weights(cfg, seed=0, gain_std=0.0)
     Ks, S = (1, 2, 4, 8, 16), args.sweep_steps
     patterns = (("all-accept", None), ("reject-slot-0", 0), ("reject-slot-K/2", "mid"))
@@ -573,7 +583,7 @@ def run_ours(args):
     cfg = model_config(args)
     K, W, S = args.K, args.warmup, args.steps
     hbm_peak, peak_kind = peaks()
-    stream = torch.cuda.current_stream()
+    stream = side_stream(torch)
 
     weights = inputs.device_weights(cfg, seed=0, gain_std=0.0)
     max_seq = args.prefix + GEN_TOKENS + 2 * K + 16

@@ -467,18 +467,27 @@ void release_pages(sv_ctx* ctx, int len) {
   if (keep < ctx->n_alloc) ctx->n_alloc = keep;
 }
 
-int begin_call(sv_ctx* ctx) {
-  if (ctx->async_pending) return fail(ctx, SV_E_STATE, "asynchronous calls pending: call sv_sync first");
+// The library's stream after the caller's work so far, and the caller's
+// stream after the library's work (nothing to do when they are one stream).
+int join_user_stream(sv_ctx* ctx) {
+  if (ctx->stream == ctx->user_stream) return SV_OK;
   CK(cudaEventRecord(ctx->ev, ctx->user_stream));
   CK(cudaStreamWaitEvent(ctx->stream, ctx->ev, 0));
   return SV_OK;
 }
-
-int end_call(sv_ctx* ctx) {
+int join_library_stream(sv_ctx* ctx) {
+  if (ctx->stream == ctx->user_stream) return SV_OK;
   CK(cudaEventRecord(ctx->ev, ctx->stream));
   CK(cudaStreamWaitEvent(ctx->user_stream, ctx->ev, 0));
   return SV_OK;
 }
+
+int begin_call(sv_ctx* ctx) {
+  if (ctx->async_pending) return fail(ctx, SV_E_STATE, "asynchronous calls pending: call sv_sync first");
+  return join_user_stream(ctx);
+}
+
+int end_call(sv_ctx* ctx) { return join_library_stream(ctx); }
 
 // Stage [cap_len, tokens[0..n)] at slot `at` of the pinned input buffer and
 // copy it into the device state.
@@ -559,7 +568,16 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
   cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
   if (ctx->num_sms <= 0) ctx->num_sms = 1;
   ctx->user_stream = static_cast<cudaStream_t>(cuda_stream);
-  if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess) return bail(SV_E_CUDA);
+  // A stream of the caller's is the library's too: no event join at every
+  // call (about 6 us a step on the 8B shape).  The default streams (legacy,
+  // per-thread) take no capture or programmatic dependent launch, so their
+  // callers get a stream of the library's, joined to theirs at each call.
+  const bool user_default = ctx->user_stream == nullptr || ctx->user_stream == cudaStreamLegacy ||
+                            ctx->user_stream == cudaStreamPerThread;
+  if (!user_default)
+    ctx->stream = ctx->user_stream;
+  else if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess)
+    return bail(SV_E_CUDA);
   if (cudaEventCreateWithFlags(&ctx->ev, cudaEventDisableTiming) != cudaSuccess) return bail(SV_E_CUDA);
   const char* ng = getenv("SV_NO_GRAPHS");
   ctx->use_graphs = !(ng && ng[0] == '1');
@@ -696,7 +714,7 @@ void sv_destroy(sv_ctx* ctx) {
   if (ctx->pin_out) cudaFreeHost(ctx->pin_out);
   if (ctx->pin_bt) cudaFreeHost(ctx->pin_bt);
   if (ctx->ev) cudaEventDestroy(ctx->ev);
-  if (ctx->stream) cudaStreamDestroy(ctx->stream);
+  if (ctx->stream && ctx->stream != ctx->user_stream) cudaStreamDestroy(ctx->stream);
   delete ctx;
 }
 
@@ -788,16 +806,14 @@ int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits
   if (!ctx) return SV_E_INVAL;
   if (K < 1 || K > ctx->cfg.max_k) return fail(ctx, SV_E_INVAL, "K=%d outside [1, %d]", K, ctx->cfg.max_k);
   if (!tokens_dev || !result_dev) return fail(ctx, SV_E_INVAL, "null device pointer");
-  CK(cudaEventRecord(ctx->ev, ctx->user_stream));
-  CK(cudaStreamWaitEvent(ctx->stream, ctx->ev, 0));
+  int rc = join_user_stream(ctx);
+  if (rc) return rc;
   ctx->async_pending = true;
   CK(cudaMemcpyAsync(ctx->st->tokens, tokens_dev, K * sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
-  int rc = run_step(ctx, K, MODE_VERIFY, logits_dev);
+  rc = run_step(ctx, K, MODE_VERIFY, logits_dev);
   if (rc) return rc;
   CK(cudaMemcpyAsync(result_dev, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
-  CK(cudaEventRecord(ctx->ev, ctx->stream));
-  CK(cudaStreamWaitEvent(ctx->user_stream, ctx->ev, 0));
-  return SV_OK;
+  return join_library_stream(ctx);
 }
 
 int sv_reserve(sv_ctx* ctx, int len) {

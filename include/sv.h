@@ -117,9 +117,13 @@ typedef struct {
 } sv_weights;
 
 /* Create a context on the current CUDA device.  cuda_stream: the caller's
- * stream (cudaStream_t) or NULL for the legacy stream; the library orders its
- * own internal stream after it at the start of each call and the caller's
- * stream after the library's work at the end.  Allocates the KV pool, block
+ * stream (cudaStream_t), or NULL for the legacy stream.  A stream of the
+ * caller's (not NULL, cudaStreamLegacy or cudaStreamPerThread) is the one
+ * every call of the context runs on; it must outlive the context.  For the
+ * default streams, which take no stream capture or programmatic dependent
+ * launch, the library runs on a stream of its own, ordered after the
+ * caller's stream at the start of each call and the caller's stream after
+ * the library's work at the end.  Allocates the KV pool, block
  * table, activations, workspaces and the tiled weight copies (all owned by
  * the context); it synchronises the device first, since it reads the
  * weights.
