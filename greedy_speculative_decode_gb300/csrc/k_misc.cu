@@ -12,16 +12,17 @@ namespace {
 // accept kernel commits nothing.
 __global__ void __launch_bounds__(128) k_embed(const bf16* __restrict__ E, int hidden, int vocab,
                                                bf16* __restrict__ x, float* __restrict__ x_ss,
-                                               int ss_tiles, SvState* st, int check) {
+                                               int ss_tiles, SvState* st, int check, StepIo io) {
   pdl_trigger();
   __shared__ float part[4];
   const int t = blockIdx.x, m = blockIdx.y, i = threadIdx.x;
   if (t == 0 && m == 0 && i == 0) {
     st->step_pos = st->seq_len;
     const int pending = st->pending;
-    st->step_reject = (check && pending >= 0 && st->tokens[0] != pending) ? 1 : 0;
+    const int tok0 = io.tokens ? io.tokens[0] : st->tokens[0];
+    st->step_reject = (check && pending >= 0 && tok0 != pending) ? 1 : 0;
   }
-  embed_tile(E, hidden, vocab, x, x_ss, ss_tiles, st, m, t, i, part, 3);
+  embed_tile(E, hidden, vocab, x, x_ss, ss_tiles, st, m, t, i, part, 3, io.tokens);
   // Launched as a dependent of the delayed write-through window copy, which
   // touches none of the above, this kernel ends only after the copy has: the
   // step's later kernels wait for this one.  (No-op otherwise.)
@@ -33,13 +34,14 @@ __global__ void __launch_bounds__(256) k_accept(SvState* st, const float* __rest
                                                 const int* __restrict__ am_idx, int n_tiles, int M,
                                                 int mode, bf16* kpool, bf16* vpool,
                                                 size_t layer_stride, const int* block_table,
-                                                int n_layers, int n_kv_heads, int head_dim, KvDelay dl) {
+                                                int n_layers, int n_kv_heads, int head_dim, KvDelay dl,
+                                                StepIo io) {
   pdl_trigger();
   pdl_wait();
   __shared__ int s_am[kMaxK];
   __shared__ int s_n;
   accept_work(st, am_val, am_idx, n_tiles, M, mode, kpool, vpool, layer_stride, block_table,
-              n_layers, n_kv_heads, head_dim, dl, blockIdx.x, gridDim.x, s_am, &s_n);
+              n_layers, n_kv_heads, head_dim, dl, blockIdx.x, gridDim.x, s_am, &s_n, io.result);
 }
 
 // Delayed write-through: before a verify step of M rows at pos = seq_len,
@@ -159,20 +161,66 @@ cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, cudaLaunchAtt
 }  // namespace
 
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
-                         SvState* st, bool check, cudaStream_t s, bool pdl) {
+                         SvState* st, bool check, cudaStream_t s, bool pdl, const StepIo& io) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(hidden / 128, M), dim3(128), s, attr, pdl);
-  return cudaLaunchKernelEx(&cfg, k_embed, E, hidden, vocab, x, x_ss, hidden / 128, st, check ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg, k_embed, E, hidden, vocab, x, x_ss, hidden / 128, st, check ? 1 : 0, io);
 }
 
 cudaError_t launch_accept(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                           int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                           const int* block_table, int n_layers, int n_kv_heads, int head_dim,
-                          const KvDelay& dl, cudaStream_t s, bool pdl) {
+                          const KvDelay& dl, cudaStream_t s, bool pdl, const StepIo& io) {
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = make_cfg(dim3(n_layers > 0 ? n_layers : 1), dim3(256), s, attr, pdl);
   return cudaLaunchKernelEx(&cfg, k_accept, st, am_val, am_idx, n_tiles, M, mode, kpool, vpool,
-                            layer_stride, block_table, n_layers, n_kv_heads, head_dim, dl);
+                            layer_stride, block_table, n_layers, n_kv_heads, head_dim, dl, io);
+}
+
+namespace {
+template <typename... A>
+constexpr int n_params(void (*)(A...)) {
+  return (int)sizeof...(A);
+}
+}  // namespace
+
+bool step_io_node(cudaGraphNode_t node) {
+  cudaGraphNodeType type;
+  cudaKernelNodeParams kp;
+  if (cudaGraphNodeGetType(node, &type) != cudaSuccess || type != cudaGraphNodeTypeKernel ||
+      cudaGraphKernelNodeGetParams(node, &kp) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return kp.func == reinterpret_cast<void*>(k_embed) || kp.func == reinterpret_cast<void*>(k_accept);
+}
+
+// The captured argument list with its last entry (the StepIo of both
+// kernels) replaced.
+cudaError_t set_step_io(cudaGraphExec_t exec, cudaGraphNode_t node, const StepIo& io) {
+  cudaKernelNodeParams kp;
+  cudaError_t e = cudaGraphKernelNodeGetParams(node, &kp);
+  if (e != cudaSuccess) return e;
+  constexpr int kEmbed = n_params(k_embed), kAccept = n_params(k_accept);
+  constexpr int kMax = kEmbed > kAccept ? kEmbed : kAccept;
+  int n;
+  if (kp.func == reinterpret_cast<void*>(k_embed))
+    n = kEmbed;
+  else if (kp.func == reinterpret_cast<void*>(k_accept))
+    n = kAccept;
+  else
+    return cudaErrorInvalidValue;
+  if (kp.kernelParams == nullptr || kp.extra != nullptr) return cudaErrorNotSupported;
+  // the node as captured: the state block's tokens and result
+  const StepIo* captured = static_cast<const StepIo*>(kp.kernelParams[n - 1]);
+  if (captured == nullptr || captured->tokens != nullptr || captured->result != nullptr)
+    return cudaErrorInvalidValue;
+  void* args[kMax];
+  for (int i = 0; i < n - 1; ++i) args[i] = kp.kernelParams[i];
+  StepIo v = io;
+  args[n - 1] = &v;
+  kp.kernelParams = args;
+  return cudaGraphExecKernelNodeSetParams(exec, node, &kp);
 }
 
 cudaError_t launch_kv_window_in(bf16* kpool, bf16* vpool, size_t layer_stride, const int* block_table,

@@ -13,8 +13,9 @@ namespace {
 __device__ __forceinline__ void embed_tile(const bf16* __restrict__ E, int hidden, int vocab,
                                            bf16* __restrict__ x, float* __restrict__ x_ss,
                                            int ss_tiles, SvState* st, int m, int t, int i,
-                                           float* part, int bar) {
-  int tok = st->tokens[m];
+                                           float* part, int bar, const int32_t* tok_src) {
+  int tok = tok_src ? tok_src[m] : st->tokens[m];
+  if (tok_src && t == 0 && i == 0) st->tokens[m] = tok;  // for the accept kernel
   if (tok < 0 || tok >= vocab) {
     if (i == 0) atomicOr(&st->status, ST_BAD_TOKEN);
     tok = 0;
@@ -47,16 +48,27 @@ __device__ __forceinline__ void embed_tile(const bf16* __restrict__ E, int hidde
 __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                             int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                             const int* block_table, int n_layers, int n_kv_heads, int head_dim,
-                            const KvDelay& dl, int cta, int G_ctas, int* s_am, int* s_n) {
+                            const KvDelay& dl, int cta, int G_ctas, int* s_am, int* s_n,
+                            int32_t* res_dst) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int pos = __ldcg(&st->step_pos);
+  // the step's result, into the state block and, if given, the caller's buffer
+  auto put_result = [&](int a, int b, int c, int d) {
+    st->result[0] = a;
+    st->result[1] = b;
+    st->result[2] = c;
+    st->result[3] = d;
+    if (res_dst) {  // 4-byte aligned only
+      res_dst[0] = a;
+      res_dst[1] = b;
+      res_dst[2] = c;
+      res_dst[3] = d;
+    }
+  };
   if (mode == MODE_BODY) {
     if (cta == 0 && tid == 0) {
       st->seq_len = pos + M;
-      st->result[0] = M - 1;
-      st->result[1] = -1;
-      st->result[2] = pos + M;
-      st->result[3] = st->status;
+      put_result(M - 1, -1, pos + M, st->status);
     }
     return;
   }
@@ -108,17 +120,11 @@ __device__ void accept_work(SvState* st, const float* am_val, const int* am_idx,
     for (int r = 0; r < M; ++r) st->argmax[r] = s_am[r];
     st->seq_len = new_len;
     if (reject) {
-      st->result[0] = -1;
-      st->result[1] = st->pending;
-      st->result[2] = new_len;
-      st->result[3] = st->status | ST_BAD_STATE;
+      put_result(-1, st->pending, new_len, st->status | ST_BAD_STATE);
       st->state_err = 1;
     } else {
       st->pending = s_am[n];
-      st->result[0] = n;
-      st->result[1] = s_am[n];
-      st->result[2] = new_len;
-      st->result[3] = st->status;
+      put_result(n, s_am[n], new_len, st->status);
     }
   }
   // K/V rows move in 16-byte vectors: a row of one kv head is head_dim

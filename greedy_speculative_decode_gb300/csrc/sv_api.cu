@@ -19,7 +19,11 @@ using namespace sv;
 struct GraphEntry {
   int M, mode;
   float* logits;
+  cudaGraph_t graph;  // kept: its nodes name the ones of `exec` to update
   cudaGraphExec_t exec;
+  cudaGraphNode_t io_nodes[2];  // the embedding and accept nodes (both or none)
+  int n_io;
+  StepIo io;  // what those nodes take now
 };
 
 struct sv_ctx {
@@ -320,7 +324,7 @@ AttnParams attn_params(sv_ctx* ctx, int l, int M, int mode) {
 }
 
 // Enqueue every kernel of one step of M rows on ctx->stream.
-int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
+int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits, const StepIo& io) {
   const sv_config& c = ctx->cfg;
   const int H = c.hidden, d = c.head_dim, Hkv = c.n_kv_heads;
   cudaStream_t s = ctx->stream;
@@ -336,7 +340,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
   // at a time: see sv_prefill)
   if (M <= kMaxK)
     CK(launch_embed(ctx->embed, H, c.vocab, M, ctx->x, ctx->x_ss, ctx->st, mode == MODE_VERIFY, s,
-                    pdl && dl.bt_shadow != nullptr));
+                    pdl && dl.bt_shadow != nullptr, io));
   auto trace_copy = [&](int entry) -> cudaError_t {
     if (!tracing) return cudaSuccess;
     return cudaMemcpyAsync(ctx->trace + (size_t)entry * M * H, ctx->x, (size_t)M * H * sizeof(bf16),
@@ -397,24 +401,31 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits) {
     CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_HEAD, 0)));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
-                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, dl, s, pdl));
+                   ctx->vpool, ctx->layer_stride, ctx->block_table, c.n_layers, Hkv, d, dl, s, pdl, io));
   return SV_OK;
 }
 
-// Run one step: replay (capturing on first use) the graph of this shape.
-int run_step(sv_ctx* ctx, int M, int mode, float* logits) {
-  if (!ctx->use_graphs || ctx->trace) return enqueue_step(ctx, M, mode, logits);
-  for (auto& g : ctx->graphs)
+void destroy_graphs(sv_ctx* ctx) {
+  for (auto& g : ctx->graphs) {
+    cudaGraphExecDestroy(g.exec);
+    cudaGraphDestroy(g.graph);
+  }
+  ctx->graphs.clear();
+}
+
+// The graph of this step shape, captured on first use (with the state
+// block's tokens and result: StepIo{}).  Returns its index in ctx->graphs.
+int step_graph(sv_ctx* ctx, int M, int mode, float* logits, size_t* index) {
+  for (size_t i = 0; i < ctx->graphs.size(); ++i) {
+    const GraphEntry& g = ctx->graphs[i];
     if (g.M == M && g.mode == mode && g.logits == logits) {
-      CK(cudaGraphLaunch(g.exec, ctx->stream));
+      *index = i;
       return SV_OK;
     }
-  if (ctx->graphs.size() >= 64) {
-    for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.exec);
-    ctx->graphs.clear();
   }
+  if (ctx->graphs.size() >= 64) destroy_graphs(ctx);
   CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
-  int rc = enqueue_step(ctx, M, mode, logits);
+  int rc = enqueue_step(ctx, M, mode, logits, StepIo{});
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(ctx->stream, &graph);
   if (rc != SV_OK) {
@@ -422,12 +433,50 @@ int run_step(sv_ctx* ctx, int M, int mode, float* logits) {
     return rc;
   }
   if (e != cudaSuccess) return fail(ctx, SV_E_CUDA, "stream capture failed: %s", cudaGetErrorString(e));
-  cudaGraphExec_t exec = nullptr;
-  e = cudaGraphInstantiate(&exec, graph, 0);
-  cudaGraphDestroy(graph);
-  if (e != cudaSuccess) return fail(ctx, SV_E_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
-  ctx->graphs.push_back({M, mode, logits, exec});
-  CK(cudaGraphLaunch(exec, ctx->stream));
+  GraphEntry g = {M, mode, logits, graph, nullptr, {nullptr, nullptr}, 0, StepIo{}};
+  size_t n = 0;
+  std::vector<cudaGraphNode_t> nodes;
+  if (cudaGraphGetNodes(graph, nullptr, &n) == cudaSuccess) {
+    nodes.resize(n);
+    if (cudaGraphGetNodes(graph, nodes.data(), &n) != cudaSuccess) nodes.clear();
+  }
+  cudaGetLastError();
+  for (cudaGraphNode_t node : nodes)
+    if (step_io_node(node) && g.n_io < 2) g.io_nodes[g.n_io++] = node;
+  if (g.n_io != 2) g.n_io = 0;  // (a block of more than kMaxK rows has no embedding node)
+  e = cudaGraphInstantiate(&g.exec, graph, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return fail(ctx, SV_E_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  }
+  ctx->graphs.push_back(g);
+  *index = ctx->graphs.size() - 1;
+  return SV_OK;
+}
+
+// Whether a step of this shape can take its tokens and result from and to
+// the caller's buffers (StepIo) instead of the state block.
+bool step_takes_io(sv_ctx* ctx, int M, int mode, float* logits) {
+  if (!ctx->use_graphs || ctx->trace) return true;
+  size_t i = 0;
+  if (step_graph(ctx, M, mode, logits, &i) != SV_OK) return false;  // run_step reports it
+  return ctx->graphs[i].n_io == 2;
+}
+
+// Run one step: replay (capturing on first use) the graph of this shape,
+// its embedding and accept nodes pointed at `io` first where they differ.
+int run_step(sv_ctx* ctx, int M, int mode, float* logits, const StepIo& io = StepIo{}) {
+  if (!ctx->use_graphs || ctx->trace) return enqueue_step(ctx, M, mode, logits, io);
+  size_t i = 0;
+  int rc = step_graph(ctx, M, mode, logits, &i);
+  if (rc) return rc;
+  GraphEntry& g = ctx->graphs[i];
+  if (g.io.tokens != io.tokens || g.io.result != io.result) {
+    if (g.n_io != 2) return fail(ctx, SV_E_INVAL, "this step's graph takes no caller buffers");
+    for (int k = 0; k < 2; ++k) CK(set_step_io(g.exec, g.io_nodes[k], io));
+    g.io = io;
+  }
+  CK(cudaGraphLaunch(g.exec, ctx->stream));
   return SV_OK;
 }
 
@@ -708,7 +757,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
 void sv_destroy(sv_ctx* ctx) {
   if (!ctx) return;
   if (ctx->stream) cudaStreamSynchronize(ctx->stream);
-  for (auto& g : ctx->graphs) cudaGraphExecDestroy(g.exec);
+  destroy_graphs(ctx);
   for (void* p : ctx->allocs) cudaFree(p);
   if (ctx->pin_in) cudaFreeHost(ctx->pin_in);
   if (ctx->pin_out) cudaFreeHost(ctx->pin_out);
@@ -786,7 +835,7 @@ int sv_prefill(sv_ctx* ctx, const int32_t* tokens_host, int n, float* last_logit
         if ((rc = upload_tokens(ctx, tokens_host + done + r, mr, at))) return rc;
         at += mr + 1;
         CK(launch_embed(ctx->embed, H, ctx->cfg.vocab, mr, ctx->x + (size_t)r * H,
-                        ctx->x_ss + (size_t)r * (H / 128), ctx->st, false, ctx->stream, false));
+                        ctx->x_ss + (size_t)r * (H / 128), ctx->st, false, ctx->stream, false, StepIo{}));
       }
     } else {
       if ((rc = upload_tokens(ctx, tokens_host + done, M, at))) return rc;
@@ -806,9 +855,24 @@ int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits
   if (!ctx) return SV_E_INVAL;
   if (K < 1 || K > ctx->cfg.max_k) return fail(ctx, SV_E_INVAL, "K=%d outside [1, %d]", K, ctx->cfg.max_k);
   if (!tokens_dev || !result_dev) return fail(ctx, SV_E_INVAL, "null device pointer");
+  for (const void* ptr : {static_cast<const void*>(tokens_dev), static_cast<const void*>(result_dev)}) {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, ptr) != cudaSuccess ||
+        (pa.type != cudaMemoryTypeDevice && pa.type != cudaMemoryTypeManaged) || pa.device != ctx->device) {
+      cudaGetLastError();
+      return fail(ctx, SV_E_INVAL, "tokens_dev and result_dev must be memory of the context's device");
+    }
+  }
   int rc = join_user_stream(ctx);
   if (rc) return rc;
   ctx->async_pending = true;
+  // The step's graph reads the tokens and writes the result in the caller's
+  // buffers itself (its embedding and accept nodes re-pointed), saving a copy
+  // on each side of it; otherwise the state block takes them by copies.
+  if (step_takes_io(ctx, K, MODE_VERIFY, logits_dev)) {
+    if ((rc = run_step(ctx, K, MODE_VERIFY, logits_dev, StepIo{tokens_dev, result_dev}))) return rc;
+    return join_library_stream(ctx);
+  }
   CK(cudaMemcpyAsync(ctx->st->tokens, tokens_dev, K * sizeof(int32_t), cudaMemcpyDeviceToDevice, ctx->stream));
   rc = run_step(ctx, K, MODE_VERIFY, logits_dev);
   if (rc) return rc;

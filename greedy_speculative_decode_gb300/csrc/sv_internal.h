@@ -206,15 +206,28 @@ size_t linear_smem_bytes(int mt);
 cudaError_t launch_attention(const CUtensorMap& kmap, const CUtensorMap& vmap, const AttnParams& p,
                              int head_dim, int grid, bool multi, cudaStream_t s, bool pdl);
 cudaError_t launch_attn_combine(const AttnParams& p, int head_dim, cudaStream_t s, bool pdl);
+// Where a step takes its tokens and leaves its result besides the state
+// block: the asynchronous verify call's device buffers of the caller, read by
+// the embedding kernel (which copies them into st->tokens for the accept
+// kernel) and written by the accept kernel.  Null: st->tokens, st->result only.
+struct StepIo {
+  const int32_t* tokens;  // [M]
+  int32_t* result;        // [4]
+};
 // check: a verify step, whose tokens[0] must equal st->pending when that is known.
 // pdl: launched as a programmatic dependent of the delayed write-through
 // window copy (the kernel then ends only after the copy has).
 cudaError_t launch_embed(const bf16* E, int hidden, int vocab, int M, bf16* x, float* x_ss,
-                         SvState* st, bool check, cudaStream_t s, bool pdl);
+                         SvState* st, bool check, cudaStream_t s, bool pdl, const StepIo& io);
 cudaError_t launch_accept(SvState* st, const float* am_val, const int* am_idx, int n_tiles, int M,
                           int mode, bf16* kpool, bf16* vpool, size_t layer_stride,
                           const int* block_table, int n_layers, int n_kv_heads, int head_dim,
-                          const KvDelay& dl, cudaStream_t s, bool pdl);
+                          const KvDelay& dl, cudaStream_t s, bool pdl, const StepIo& io);
+// A captured step graph's embedding and accept nodes: step_io_node tells
+// whether `node` runs one of the two; set_step_io gives such a node, in the
+// instantiated `exec`, the StepIo `io` (its other arguments as captured).
+bool step_io_node(cudaGraphNode_t node);
+cudaError_t set_step_io(cudaGraphExec_t exec, cudaGraphNode_t node, const StepIo& io);
 // Delayed write-through, before a verify step of M rows: map the window's
 // pages to the scratch pages in the shadow table and copy the real pages'
 // contents there (zeros for pages not yet held).
