@@ -222,7 +222,6 @@ def ncu_traffic():
     return None
 
 
-# ------------------------------------------------------------------ CPU oracle
 def side_stream(torch):
     """A stream of its own, made current: the library then runs on it
     directly (on the default stream it would run on one of its own, joined
@@ -233,6 +232,7 @@ def side_stream(torch):
     return s
 
 
+# ------------------------------------------------------------------ CPU oracle
 def expected_tokens_per_step(K, p):
     """E[n + 1] when each draft slot matches with probability 1 - p and
     acceptance stops at the first mismatch: 1 + q + ... + q^(K-1)."""
