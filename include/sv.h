@@ -185,7 +185,10 @@ int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev,
 /* Asynchronous verify with device-resident input and output, for callers that
  * keep drafts on the GPU (the same step as sv_verify).  tokens_dev: int32 [K];
  * result_dev: int32 [4] = {n_accepted, correction_token, new_length, status
- * (0 = ok)}.  The sequence length and pending token are tracked on the
+ * (0 = ok)}; both memory of the context's device (else SV_E_INVAL, nothing
+ * queued), 4-byte aligned, read and written by the step's kernels themselves
+ * (so they must stay valid until the step is done).  The sequence length and
+ * pending token are tracked on the
  * device; pages must already cover every position the call writes (see
  * sv_reserve), otherwise the kernels skip the writes and report a nonzero
  * status.  A step whose tokens[0] is not the pending token commits nothing:
