@@ -34,7 +34,7 @@ namespace {
 // range boundaries is finished by the last of its CTAs to arrive, which sums
 // the per-CTA partials in k order.  The partition depends only on the weight
 // shape and the grid (one CTA per SM), never on M.
-template <int MT, int EPI, bool NORM>
+template <int MT, int EPI, bool NORM, int SB>
 __global__ void __launch_bounds__(kLinThreads, 1)
     k_linear(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap pfmap,
              const LinParams p) {
@@ -67,15 +67,15 @@ __global__ void __launch_bounds__(kLinThreads, 1)
     return;
   }
   // (the consumers wait for the previous kernel inside, after the work that does not need it)
-  if (!lin_consume<MT, EPI, NORM>(p, blockIdx.x, gridDim.x, sm, it) && lane == 0)
+  if (!lin_consume<MT, EPI, NORM, SB>(p, blockIdx.x, gridDim.x, sm, it) && lane == 0)
     atomicOr(&p.st->status, ST_TIMEOUT);
 }
 
-template <int MT, int EPI, bool NORM>
+template <int MT, int EPI, bool NORM, int SB>
 cudaError_t launch_t(const LinearDesc& d, const LinParams& p, cudaStream_t s, bool pdl,
                      const CUtensorMap& pfmap) {
   const size_t smem = linear_smem_bytes(MT);
-  auto kern = k_linear<MT, EPI, NORM>;
+  auto kern = k_linear<MT, EPI, NORM, SB>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(d.grid);
   cfg.blockDim = dim3(kLinThreads);
@@ -89,35 +89,46 @@ cudaError_t launch_t(const LinearDesc& d, const LinParams& p, cudaStream_t s, bo
   return cudaLaunchKernelEx(&cfg, kern, d.map, pfmap, p);
 }
 
-template <int MT, int EPI, bool NORM>
+template <int MT, int EPI, bool NORM, int SB>
 cudaError_t prepare_t() {
-  return cudaFuncSetAttribute(k_linear<MT, EPI, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(k_linear<MT, EPI, NORM, SB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)linear_smem_bytes(MT));
+}
+
+template <int MT, int SB>
+cudaError_t prepare_sb() {
+  cudaError_t e;
+  if ((e = prepare_t<MT, EPI_QKV, true, SB>()) != cudaSuccess) return e;
+  if ((e = prepare_t<MT, EPI_RESID, false, SB>()) != cudaSuccess) return e;
+  if ((e = prepare_t<MT, EPI_GLU, true, SB>()) != cudaSuccess) return e;
+  return prepare_t<MT, EPI_LOGITS, true, SB>();
+}
+
+template <int MT, int SB>
+cudaError_t launch_sb(const LinearDesc& d, const LinParams& p, int epi, bool norm, cudaStream_t s,
+                      bool pdl, const CUtensorMap& pf) {
+  switch (epi) {
+    case EPI_QKV:
+      return norm ? launch_t<MT, EPI_QKV, true, SB>(d, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_RESID:
+      return norm ? cudaErrorInvalidValue : launch_t<MT, EPI_RESID, false, SB>(d, p, s, pdl, pf);
+    case EPI_GLU:
+      return norm ? launch_t<MT, EPI_GLU, true, SB>(d, p, s, pdl, pf) : cudaErrorInvalidValue;
+    case EPI_LOGITS:
+      return norm ? launch_t<MT, EPI_LOGITS, true, SB>(d, p, s, pdl, pf) : cudaErrorInvalidValue;
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <int MT>
 cudaError_t prepare_mt() {
-  cudaError_t e;
-  if ((e = prepare_t<MT, EPI_QKV, true>()) != cudaSuccess) return e;
-  if ((e = prepare_t<MT, EPI_RESID, false>()) != cudaSuccess) return e;
-  if ((e = prepare_t<MT, EPI_GLU, true>()) != cudaSuccess) return e;
-  return prepare_t<MT, EPI_LOGITS, true>();
+  return prepare_sb<MT, lin_seg_batch(MT, kLinMaxSeg)>();
 }
 
 template <int MT>
 cudaError_t launch_mt(const LinearDesc& d, const LinParams& p, int epi, bool norm, cudaStream_t s,
                       bool pdl, const CUtensorMap& pf) {
-  switch (epi) {
-    case EPI_QKV:
-      return norm ? launch_t<MT, EPI_QKV, true>(d, p, s, pdl, pf) : cudaErrorInvalidValue;
-    case EPI_RESID:
-      return norm ? cudaErrorInvalidValue : launch_t<MT, EPI_RESID, false>(d, p, s, pdl, pf);
-    case EPI_GLU:
-      return norm ? launch_t<MT, EPI_GLU, true>(d, p, s, pdl, pf) : cudaErrorInvalidValue;
-    case EPI_LOGITS:
-      return norm ? launch_t<MT, EPI_LOGITS, true>(d, p, s, pdl, pf) : cudaErrorInvalidValue;
-  }
-  return cudaErrorInvalidValue;
+  return launch_sb<MT, lin_seg_batch(MT, kLinMaxSeg)>(d, p, epi, norm, s, pdl, pf);
 }
 
 }  // namespace
@@ -180,6 +191,7 @@ void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg)
 cudaError_t prepare_linear_kernels() {
   cudaError_t e;
   if ((e = prepare_mt<1>()) != cudaSuccess) return e;
+  if ((e = prepare_sb<1, 4>()) != cudaSuccess) return e;  // (prepare_mt<1>: the batch of 6)
   if ((e = prepare_mt<2>()) != cudaSuccess) return e;
   return prepare_mt<4>();
 }
@@ -200,7 +212,9 @@ cudaError_t launch_linear(const LinearDesc& d, const LinParams& p_in, int epi, b
     p.pf_wt = nullptr;
   }
   const CUtensorMap& pf = next ? next->map : d.map;
-  if (p.M <= 8) return launch_mt<1>(d, p, epi, norm, s, pdl, pf);
+  if (p.M <= 8)  // the gather batch of the weight's partition (the same for every M)
+    return lin_seg_batch(1, d.max_seg) == 4 ? launch_sb<1, 4>(d, p, epi, norm, s, pdl, pf)
+                                            : launch_sb<1, 6>(d, p, epi, norm, s, pdl, pf);
   if (p.M <= 16) return launch_mt<2>(d, p, epi, norm, s, pdl, pf);
   if (p.M <= 32) return launch_mt<4>(d, p, epi, norm, s, pdl, pf);
   return cudaErrorInvalidValue;
