@@ -191,7 +191,7 @@ void linear_partition(int n_tiles, int Kd, int num_sms, int* grid, int* max_seg)
 cudaError_t prepare_linear_kernels() {
   cudaError_t e;
   if ((e = prepare_mt<1>()) != cudaSuccess) return e;
-  if ((e = prepare_sb<1, 4>()) != cudaSuccess) return e;  // (prepare_mt<1>: the batch of 6)
+  if ((e = prepare_sb<1, 4>()) != cudaSuccess || (e = prepare_sb<1, 2>()) != cudaSuccess) return e;  // (prepare_mt<1>: the batch of 6)
   if ((e = prepare_mt<2>()) != cudaSuccess) return e;
   return prepare_mt<4>();
 }
@@ -213,7 +213,8 @@ cudaError_t launch_linear(const LinearDesc& d, const LinParams& p_in, int epi, b
   }
   const CUtensorMap& pf = next ? next->map : d.map;
   if (p.M <= 8)  // the gather batch of the weight's partition (the same for every M)
-    return lin_seg_batch(1, d.max_seg) == 4 ? launch_sb<1, 4>(d, p, epi, norm, s, pdl, pf)
+    return lin_seg_batch(1, d.max_seg) == 2 ? launch_sb<1, 2>(d, p, epi, norm, s, pdl, pf)
+           : lin_seg_batch(1, d.max_seg) == 4 ? launch_sb<1, 4>(d, p, epi, norm, s, pdl, pf)
                                             : launch_sb<1, 6>(d, p, epi, norm, s, pdl, pf);
   if (p.M <= 16) return launch_mt<2>(d, p, epi, norm, s, pdl, pf);
   if (p.M <= 32) return launch_mt<4>(d, p, epi, norm, s, pdl, pf);

@@ -375,12 +375,16 @@ __device__ __forceinline__ void ld_relaxed_v2_u32(const uint32_t* p, uint32_t& a
 }
 
 // Split-tile segments the reducer requests at once: three for 16 padded rows,
-// one for 32; for 8, four or six (eight or twelve word pairs a thread),
-// whichever takes a tile's other segments in fewer rounds, four on a tie (the
-// smaller batch is the cheaper code: measured 2-4% faster on the 0.6B- and
-// Gemma-shaped steps).  The sums and their order do not depend on it.
+// one for 32; for 8, the smallest of two, four or six (4, 8 or 12 word pairs
+// a thread) that takes a tile's other max_seg - 1 segments in the fewest
+// rounds: the smaller batch is the cheaper code (measured 1-5% faster steps on
+// the 0.6B- and Gemma-shaped models, 0.5% on the 8B-shaped one).  The sums and
+// their order do not depend on it.
 __host__ __device__ constexpr int lin_seg_batch(int mt, int max_seg) {
-  return mt == 2 ? 3 : mt == 4 ? 1 : ((max_seg + 2) / 4 <= (max_seg + 4) / 6 ? 4 : 6);
+  return mt == 2 ? 3
+         : mt == 4 ? 1
+         : max_seg <= 3 ? 2
+         : ((max_seg + 2) / 4 <= (max_seg + 4) / 6 ? 4 : 6);
 }
 
 // Reducer side of a split tile: acc holds segment 0 (this CTA's); add the
