@@ -599,11 +599,12 @@ cudaError_t launch_tc_t(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* 
   return cudaLaunchKernelEx(&cfg, k_linear_tc<EPI, NORM, MP>, d.map, pfmap, xmap, p, slots);
 }
 
-// RMS-normalised input rows for the 128-row form: xn[m, :] =
-// bf16(bf16(x[m, :] rstd_m) gain), rstd_m from the per-128-column sums of
-// squares in tc_row_rstd's order (lane-strided sums, then an xor tree), so
-// xn holds exactly the values the norm prologue would write into every ring
-// stage, once instead of once per weight tile.  Block (c, m): row m, 16-byte
+// RMS-normalised input rows for the tcgen05 form (steps of more than 8
+// rows): xn[m, :] = bf16(bf16(x[m, :] rstd_m) gain), rstd_m from the
+// per-128-column sums of squares in tc_row_rstd's order (lane-strided sums,
+// then an xor tree), so xn holds exactly the values the norm prologue would
+// write (into every ring stage, for 128-row blocks), once per linear instead
+// of once per CTA or weight tile.  Block (c, m): row m, 16-byte
 // vectors c * 256 + threadIdx.x, ...
 __global__ void __launch_bounds__(256) k_norm_rows(const bf16* __restrict__ x, const float* __restrict__ x_ss,
                                                    const bf16* __restrict__ gain, bf16* __restrict__ xn, int H,
@@ -642,8 +643,11 @@ cudaError_t prepare_tc_t() {
   if constexpr (EPI == EPI_LOGITS) {
     return cudaSuccess;  // the LM head runs on at most 32 rows
   } else {
-    if constexpr (NORM)  // 128-row blocks take their rows normalised by k_norm_rows
+    if constexpr (NORM) {  // the step's rows come normalised by k_norm_rows (QKV, gate|up)
       if ((e = prepare_tc_mp<EPI, false, 128>()) != cudaSuccess) return e;
+      if ((e = prepare_tc_mp<EPI, false, 16>()) != cudaSuccess) return e;
+      if ((e = prepare_tc_mp<EPI, false, 32>()) != cudaSuccess) return e;
+    }
     return prepare_tc_mp<EPI, NORM, 128>();
   }
 }
@@ -653,15 +657,14 @@ cudaError_t launch_tc_mp(const LinearDesc& d, const CUtensorMap& xmap, uint32_t*
                          int epi, bool norm, cudaStream_t s, bool pdl, const CUtensorMap& pf) {
   switch (epi) {
     case EPI_QKV:
-      if constexpr (MP == 128)  // the 128-row form also takes pre-normalised rows
-        if (!norm) return launch_tc_t<EPI_QKV, false, MP>(d, xmap, slots, p, s, pdl, pf);
-      return norm ? launch_tc_t<EPI_QKV, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
+      // (rows normalised by k_norm_rows, or here in the prologue)
+      return norm ? launch_tc_t<EPI_QKV, true, MP>(d, xmap, slots, p, s, pdl, pf)
+                  : launch_tc_t<EPI_QKV, false, MP>(d, xmap, slots, p, s, pdl, pf);
     case EPI_RESID:
       return norm ? cudaErrorInvalidValue : launch_tc_t<EPI_RESID, false, MP>(d, xmap, slots, p, s, pdl, pf);
     case EPI_GLU:
-      if constexpr (MP == 128)
-        if (!norm) return launch_tc_t<EPI_GLU, false, MP>(d, xmap, slots, p, s, pdl, pf);
-      return norm ? launch_tc_t<EPI_GLU, true, MP>(d, xmap, slots, p, s, pdl, pf) : cudaErrorInvalidValue;
+      return norm ? launch_tc_t<EPI_GLU, true, MP>(d, xmap, slots, p, s, pdl, pf)
+                  : launch_tc_t<EPI_GLU, false, MP>(d, xmap, slots, p, s, pdl, pf);
     case EPI_LOGITS:  // the LM head runs on at most 32 rows
       if (MP > 32) return cudaErrorInvalidValue;
       return norm ? launch_tc_t<EPI_LOGITS, true, (MP > 32 ? 32 : MP)>(d, xmap, slots, p, s, pdl, pf)
