@@ -640,10 +640,11 @@ cudaError_t prepare_tc_t() {
   cudaError_t e;
   if ((e = prepare_tc_mp<EPI, NORM, 16>()) != cudaSuccess) return e;
   if ((e = prepare_tc_mp<EPI, NORM, 32>()) != cudaSuccess) return e;
-  if constexpr (EPI == EPI_LOGITS) {
-    return cudaSuccess;  // the LM head runs on at most 32 rows
+  if constexpr (EPI == EPI_LOGITS) {  // the LM head runs on at most 32 rows
+    if ((e = prepare_tc_mp<EPI, false, 16>()) != cudaSuccess) return e;
+    return prepare_tc_mp<EPI, false, 32>();
   } else {
-    if constexpr (NORM) {  // the step's rows come normalised by k_norm_rows (QKV, gate|up)
+    if constexpr (NORM) {  // the step's rows may come normalised by k_norm_rows
       if ((e = prepare_tc_mp<EPI, false, 128>()) != cudaSuccess) return e;
       if ((e = prepare_tc_mp<EPI, false, 16>()) != cudaSuccess) return e;
       if ((e = prepare_tc_mp<EPI, false, 32>()) != cudaSuccess) return e;
@@ -668,7 +669,7 @@ cudaError_t launch_tc_mp(const LinearDesc& d, const CUtensorMap& xmap, uint32_t*
     case EPI_LOGITS:  // the LM head runs on at most 32 rows
       if (MP > 32) return cudaErrorInvalidValue;
       return norm ? launch_tc_t<EPI_LOGITS, true, (MP > 32 ? 32 : MP)>(d, xmap, slots, p, s, pdl, pf)
-                  : cudaErrorInvalidValue;
+                  : launch_tc_t<EPI_LOGITS, false, (MP > 32 ? 32 : MP)>(d, xmap, slots, p, s, pdl, pf);
   }
   return cudaErrorInvalidValue;
 }

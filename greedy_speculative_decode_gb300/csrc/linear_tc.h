@@ -21,8 +21,8 @@ cudaError_t prepare_linear_tc_kernels();
 // (p.ws is not used), d.grid x 128 x kTcMaxRows 32-bit words, every byte 0xff
 // before the first launch; each launch leaves them so.
 // xn[m, :] = the RMS-normalised row m of x (m < M), exactly as the norm
-// prologue computes it; for steps of more than 8 rows, whose QKV and gate|up
-// linears then take xn without a norm prologue.
+// prologue computes it; for steps of more than 8 rows, whose QKV, gate|up
+// and LM head linears then take xn without a norm prologue.
 cudaError_t launch_norm_rows(const bf16* x, const float* x_ss, const bf16* gain, bf16* xn, int M, int H,
                              float eps, cudaStream_t s, bool pdl);
 cudaError_t launch_linear_tc(const LinearDesc& d, const CUtensorMap& xmap, uint32_t* slots, const LinParams& p,

@@ -372,9 +372,10 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits, const StepIo& io) 
     }
   };
   // Steps of more than 8 rows (the tcgen05 form) normalise the input rows of
-  // QKV and gate|up once, in a kernel of their own, instead of in every CTA's
-  // prologue (and, for 128-row blocks, every ring stage): the same values
-  // (k_norm_rows).  On the 8B shape K=16 3408 -> 3377 us, K=32 4258 -> 3972.
+  // QKV, gate|up and the LM head once, in a kernel of their own, instead of
+  // in every CTA's prologue (and at every restage of the input window, or for
+  // 128-row blocks every ring stage): the same values (k_norm_rows).  On the
+  // 8B shape K=16 3408 -> 3374 us, K=32 4258 -> 3960.
   auto prenorm = [&](LinParams& p, bool& nm) -> cudaError_t {
     if (M <= 8 || !nm || !ctx->use_tc) return cudaSuccess;
     cudaError_t e = launch_norm_rows(p.X, p.x_ss, p.gain, ctx->xn, M, H, c.rms_eps, s, pdl);
@@ -399,6 +400,7 @@ int enqueue_step(sv_ctx* ctx, int M, int mode, float* logits, const StepIo& io) 
   }
   if (head) {  // final RMSNorm + LM head + per-tile argmax
     LinParams p = lin_params(ctx, LIN_HEAD, 0, M, mode, logits, &epi, &norm, &ld);
+    CK(prenorm(p, norm));
     CK(run_linear(ctx, *ld, p, epi, norm, s, pdl, next_of(LIN_HEAD, 0)));
   }
   CK(launch_accept(ctx->st, ctx->am_val, ctx->am_idx, ctx->lin_head.n_tiles, M, mode, ctx->kpool,
