@@ -68,6 +68,11 @@ struct sv_ctx {
   int32_t* pin_in = nullptr;   // [cap_len, tokens...] per row block of one call
   size_t pin_in_len = 0;       // ints: max_seq + one cap_len slot per block of a full prefill
   SvState* pin_out = nullptr;  // read-back of the device state
+  // the same two as the kernels address them (pinned host memory is mapped
+  // under unified addressing); null: the synchronous verify copies instead
+  int32_t* pin_in_dev = nullptr;
+  SvState* pin_out_dev = nullptr;
+  int dev_cap = -1;  // st->cap_len as last set by the host (-1: not known)
   int* pin_bt = nullptr;       // block table mirror
   // test hook: the residual stream of each step's rows after every layer
   bf16* trace = nullptr;  // [n_layers + 1][rows][hidden]
@@ -551,6 +556,23 @@ int upload_tokens(sv_ctx* ctx, const int32_t* tokens, int n, int at) {
   memcpy(src + 1, tokens, n * sizeof(int32_t));
   CK(cudaMemcpyAsync(&ctx->st->cap_len, src, (n + 1) * sizeof(int32_t), cudaMemcpyHostToDevice,
                      ctx->stream));
+  ctx->dev_cap = src[0];
+  return SV_OK;
+}
+
+// A synchronous verify step's input without a copy of the tokens: they go
+// into the pinned staging that the embedding kernel reads (StepIo); cap_len
+// is copied only when it changed.  The previous call has finished with the
+// staging (every synchronous call ends with a stream synchronisation).
+int stage_tokens_mapped(sv_ctx* ctx, const int32_t* tokens, int n) {
+  int32_t* src = ctx->pin_in;
+  memcpy(src + 1, tokens, n * sizeof(int32_t));
+  const int cap = ctx->n_alloc * kPage;
+  if (cap != ctx->dev_cap) {
+    src[0] = cap;
+    CK(cudaMemcpyAsync(&ctx->st->cap_len, src, sizeof(int32_t), cudaMemcpyHostToDevice, ctx->stream));
+    ctx->dev_cap = cap;
+  }
   return SV_OK;
 }
 
@@ -562,9 +584,11 @@ int check_tokens(sv_ctx* ctx, const int32_t* t, int n) {
   return SV_OK;
 }
 
-int finish_sync_step(sv_ctx* ctx, int32_t* result) {
-  CK(cudaMemcpyAsync(ctx->pin_out->result, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost,
-                     ctx->stream));
+// mapped: the accept kernel wrote the result into the pinned read-back itself.
+int finish_sync_step(sv_ctx* ctx, int32_t* result, bool mapped = false) {
+  if (!mapped)
+    CK(cudaMemcpyAsync(ctx->pin_out->result, ctx->st->result, 4 * sizeof(int32_t), cudaMemcpyDeviceToHost,
+                       ctx->stream));
   CK(cudaStreamSynchronize(ctx->stream));
   memcpy(result, ctx->pin_out->result, 4 * sizeof(int32_t));
   if (result[3] & ~ST_BAD_STATE)
@@ -743,6 +767,17 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       cudaMallocHost(&ctx->pin_out, sizeof(SvState)) != cudaSuccess ||
       cudaMallocHost(&ctx->pin_bt, sizeof(int) * (size_t)ctx->bt_len) != cudaSuccess)
     return bail(SV_E_NOMEM);
+  // the device's addresses of the staging (unified addressing maps pinned
+  // host memory); without them the synchronous verify copies instead
+  {
+    void *din = nullptr, *dout = nullptr;
+    if (cudaHostGetDevicePointer(&din, ctx->pin_in, 0) == cudaSuccess &&
+        cudaHostGetDevicePointer(&dout, ctx->pin_out, 0) == cudaSuccess) {
+      ctx->pin_in_dev = static_cast<int32_t*>(din);
+      ctx->pin_out_dev = static_cast<SvState*>(dout);
+    }
+    cudaGetLastError();
+  }
   for (int i = 0; i < ctx->bt_len; ++i) ctx->pin_bt[i] = -1;
   if (cudaMemcpy(ctx->block_table, ctx->pin_bt, sizeof(int) * ctx->bt_len, cudaMemcpyHostToDevice) !=
           cudaSuccess ||
@@ -754,6 +789,7 @@ int sv_create(const sv_config* cfg, const sv_weights* w, void* cuda_stream, sv_c
       launch_set_len(ctx->st, 0, 0, -1, ctx->stream) != cudaSuccess ||
       cudaStreamSynchronize(ctx->stream) != cudaSuccess)
     return bail(SV_E_CUDA);
+  ctx->dev_cap = 0;
   *out = ctx;
   return SV_OK;
 }
@@ -784,10 +820,20 @@ int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev,
     return fail(ctx, SV_E_STATE, "tokens[0] = %d is not the pending greedy token %d", tokens_host[0],
                 ctx->pending);
   if ((rc = ensure_pages(ctx, ctx->seq_len + K))) return rc;
-  if ((rc = upload_tokens(ctx, tokens_host, K, 0))) return rc;
-  if ((rc = run_step(ctx, K, MODE_VERIFY, logits_dev))) return rc;
+  // the step reads its tokens from, and writes its result into, the pinned
+  // staging itself where that is mapped and the step's graph takes buffers
+  // (StepIo): no copy on either side of the step
+  const bool mapped = ctx->pin_in_dev && step_takes_io(ctx, K, MODE_VERIFY, logits_dev);
+  if (mapped) {
+    if ((rc = stage_tokens_mapped(ctx, tokens_host, K))) return rc;
+    rc = run_step(ctx, K, MODE_VERIFY, logits_dev, StepIo{ctx->pin_in_dev + 1, ctx->pin_out_dev->result});
+  } else {
+    if ((rc = upload_tokens(ctx, tokens_host, K, 0))) return rc;
+    rc = run_step(ctx, K, MODE_VERIFY, logits_dev);
+  }
+  if (rc) return rc;
   int32_t res[4];
-  if ((rc = finish_sync_step(ctx, res))) return rc;
+  if ((rc = finish_sync_step(ctx, res, mapped))) return rc;
   if (n_accepted) *n_accepted = res[0];
   if (correction_token) *correction_token = res[1];
   return end_call(ctx);
@@ -891,6 +937,7 @@ int sv_reserve(sv_ctx* ctx, int len) {
   if ((rc = begin_call(ctx))) return rc;
   if ((rc = ensure_pages(ctx, len))) return rc;
   CK(launch_set_len(ctx->st, ctx->seq_len, ctx->n_alloc * kPage, kKeepPending, ctx->stream));
+  ctx->dev_cap = ctx->n_alloc * kPage;
   CK(cudaStreamSynchronize(ctx->stream));
   return end_call(ctx);
 }
@@ -930,6 +977,7 @@ int sv_truncate(sv_ctx* ctx, int new_len) {
   ctx->seq_len = new_len;
   release_pages(ctx, new_len);
   CK(launch_set_len(ctx->st, new_len, ctx->n_alloc * kPage, pending, ctx->stream));
+  ctx->dev_cap = ctx->n_alloc * kPage;
   CK(cudaStreamSynchronize(ctx->stream));
   return end_call(ctx);
 }
