@@ -13,7 +13,10 @@ acceptance and truncation.  Reported:
           (sv_verify_async over device-resident windows), CUDA events on
           the caller's stream around exactly --steps steps;
   e2e     the same steps through sv_verify with host token arrays and host
-          results (H2D + D2H inside the timed region), wall clock;
+          results, wall clock: the tokens (and the page capacity) go to the
+          device and the 16-byte result comes back inside the timed region
+          (read and written by the step's kernels through the context's
+          mapped pinned staging, with no separate copy);
   roofline  the dominant kernel (the gate|up linear, 52% of a layer's bytes)
           timed on the library stream, against the measured HBM peak;
   cpu_baseline  one whole verify step of the CPU oracle on the same workload.
