@@ -457,6 +457,13 @@ int step_graph(sv_ctx* ctx, int M, int mode, float* logits, size_t* index) {
     cudaGraphDestroy(graph);
     return fail(ctx, SV_E_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
   }
+  // the nodes take a new StepIo only if the runtime hands their captured
+  // arguments back; otherwise the calls fall back to copies (step_takes_io)
+  for (int k = 0; k < g.n_io; ++k)
+    if (set_step_io(g.exec, g.io_nodes[k], StepIo{}) != cudaSuccess) {
+      cudaGetLastError();
+      g.n_io = 0;
+    }
   ctx->graphs.push_back(g);
   *index = ctx->graphs.size() - 1;
   return SV_OK;
