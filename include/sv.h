@@ -188,10 +188,9 @@ int sv_verify(sv_ctx* ctx, const int32_t* tokens_host, int K, float* logits_dev,
  * (0 = ok)}; both memory of the context's device (else SV_E_INVAL, nothing
  * queued), 4-byte aligned, read and written by the step's kernels themselves
  * (so they must stay valid until the step is done).  The sequence length and
- * pending token are tracked on the
- * device; pages must already cover every position the call writes (see
- * sv_reserve), otherwise the kernels skip the writes and report a nonzero
- * status.  A step whose tokens[0] is not the pending token commits nothing:
+ * pending token are tracked on the device; pages must already cover every
+ * position the call writes (see sv_reserve), otherwise the kernels skip the
+ * writes and report a nonzero status.  A step whose tokens[0] is not the pending token commits nothing:
  * its result is {-1, pending, old length, status | 8}, and the next sv_sync
  * returns SV_E_STATE.  Call sv_sync before any synchronous call. */
 int sv_verify_async(sv_ctx* ctx, const int32_t* tokens_dev, int K, float* logits_dev,
