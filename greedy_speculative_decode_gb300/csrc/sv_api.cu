@@ -431,7 +431,10 @@ int step_graph(sv_ctx* ctx, int M, int mode, float* logits, size_t* index) {
       return SV_OK;
     }
   }
-  if (ctx->graphs.size() >= 64) destroy_graphs(ctx);
+  if (ctx->graphs.size() >= 64) {  // (launches of the cached graphs may still be queued)
+    CK(cudaStreamSynchronize(ctx->stream));
+    destroy_graphs(ctx);
+  }
   CK(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
   int rc = enqueue_step(ctx, M, mode, logits, StepIo{});
   cudaGraph_t graph = nullptr;
