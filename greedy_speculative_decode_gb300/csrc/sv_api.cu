@@ -1093,7 +1093,14 @@ int sv_spec_generate(sv_ctx* target, sv_ctx* draft, int32_t pending, int K, int 
 
 int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head) {
   if (!ctx || K < 1) return SV_E_INVAL;
-  return 1 + 6 * ctx->cfg.n_layers + (with_head ? 2 : 1) + (with_head && step_delayed(ctx, K, MODE_VERIFY) ? 1 : 0);
+  // steps of more than 8 rows normalise the input rows once per linear
+  // (enqueue_step's prenorm): before QKV and gate|up, and before the LM head
+  const bool prenorm = K > 8 && ctx->use_tc;
+  const int embeds = (K + kMaxK - 1) / kMaxK;  // larger blocks are embedded kMaxK rows a launch
+  const int per_layer = 6 + (prenorm ? 2 : 0);
+  const int tail = with_head ? 2 + (prenorm ? 1 : 0) : 1;  // [norm,] LM head, accept; or accept
+  const int window = with_head && step_delayed(ctx, K, MODE_VERIFY) ? 1 : 0;
+  return embeds + per_layer * ctx->cfg.n_layers + tail + window;
 }
 
 int sv_time_linear(sv_ctx* ctx, int which, int K, int reps, float* avg_us, double* bytes_per_launch) {

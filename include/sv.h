@@ -264,7 +264,10 @@ int sv_trace_hidden(sv_ctx* ctx, void* hidden_dev, int max_rows);
 
 /* Number of kernel launches in one step of K rows: with_head = 1 counts a
  * verify step (LM head and acceptance, and for kv_delayed with K > 1 the
- * window copy), 0 a prefill block without the LM head. */
+ * window copy), 0 a prefill block without the LM head (a block of more than
+ * 32 rows is embedded 32 rows a launch).  Steps of more than 8 rows on the
+ * tcgen05 form add one row normalisation before each QKV, gate|up and LM
+ * head linear. */
 int sv_step_kernel_count(const sv_ctx* ctx, int K, int with_head);
 
 /* The row blocks sv_prefill cuts n tokens into, in order, written to
