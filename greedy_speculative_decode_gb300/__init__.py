@@ -112,6 +112,24 @@ def _check_tensor(t, name, dtype, shape):
         raise ValueError(f"{name}: must be contiguous")
 
 
+def _check_buf(t, name, dtype, min_numel, cuda=False):
+    """A buffer that a step's kernels read or write whole (tokens, result,
+    logits): the C call sees only its address, so a buffer of another type,
+    not contiguous or too small would become out-of-bounds accesses there.
+    cuda: must also be device memory (the library checks the asynchronous
+    call's token and result buffers itself)."""
+    if t is None:
+        return
+    if cuda and not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if str(t.dtype) != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name}: {t.numel()} elements, at least {min_numel} needed")
+
+
 def lm_head_noalloc(x, gain, w, logits, argmax=None, status=None, eps=1e-6, stream=None):
     """sv_lm_head_noalloc: logits and greedy tokens of M rows without any
     device allocation by the library (scratch is a fixed array inside it).
@@ -220,18 +238,21 @@ class Context:
 
     # ----------------------------------------------------------- the calls
     def prefill(self, tokens, logits=None) -> int:
+        _check_buf(logits, "logits", "torch.float32", self.cfg.vocab, cuda=True)
         arr = _i32_array(tokens)
         nxt = ctypes.c_int32(0)
         self._check(_lib.sv_prefill(self._h, arr, len(arr), _P(_ptr(logits)), ctypes.byref(nxt)))
         return nxt.value
 
     def decode(self, token: int, logits=None) -> int:
+        _check_buf(logits, "logits", "torch.float32", self.cfg.vocab, cuda=True)
         nxt = ctypes.c_int32(0)
         self._check(_lib.sv_decode(self._h, int(token), _P(_ptr(logits)), ctypes.byref(nxt)))
         return nxt.value
 
     def verify(self, tokens, logits=None):
         arr = _i32_array(tokens)
+        _check_buf(logits, "logits", "torch.float32", len(arr) * self.cfg.vocab, cuda=True)
         n = ctypes.c_int32(0)
         c = ctypes.c_int32(0)
         self._check(_lib.sv_verify(self._h, arr, len(arr), _P(_ptr(logits)), ctypes.byref(n),
@@ -239,6 +260,9 @@ class Context:
         return n.value, c.value
 
     def verify_async(self, tokens_dev, K: int, result_dev, logits=None):
+        _check_buf(tokens_dev, "tokens_dev", "torch.int32", int(K))
+        _check_buf(result_dev, "result_dev", "torch.int32", 4)
+        _check_buf(logits, "logits", "torch.float32", int(K) * self.cfg.vocab, cuda=True)
         self._check(_lib.sv_verify_async(self._h, _P(_ptr(tokens_dev)), int(K), _P(_ptr(logits)),
                                          _P(_ptr(result_dev))))
 

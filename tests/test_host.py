@@ -163,3 +163,23 @@ def test_create_rejects_bad_kv_delayed(bad):
     h = ctypes.c_void_p(0)
     assert sv.lib().sv_create(ctypes.byref(c), ctypes.byref(w), None, ctypes.byref(h)) == sv.SV_E_INVAL
     assert not h.value
+
+
+def test_step_buffers_are_checked_before_the_call():
+    """The binding refuses a step buffer of the wrong type, layout or size
+    (the C call sees only its address); logits must also be device memory.
+    No GPU is needed: the checks run before any library call."""
+    import torch
+    import greedy_speculative_decode_gb300 as sv
+    chk = sv._check_buf
+    chk(None, "logits", "torch.float32", 10, cuda=True)                 # no buffer: nothing to check
+    chk(torch.zeros(4, dtype=torch.int32), "tokens_dev", "torch.int32", 4)  # right type and size
+    bad = [
+        (torch.zeros(4, dtype=torch.int64), "torch.int32", 4, False),      # type
+        (torch.zeros(8, dtype=torch.int32)[::2], "torch.int32", 4, False),  # layout
+        (torch.zeros(3, dtype=torch.int32), "torch.int32", 4, False),      # size
+        (torch.zeros((4, 10), dtype=torch.float32), "torch.float32", 40, True),  # host logits
+    ]
+    for t, dtype, n, cuda in bad:
+        with pytest.raises(ValueError):
+            chk(t, "buf", dtype, n, cuda=cuda)
